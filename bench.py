@@ -1,0 +1,443 @@
+"""Decode-step benchmark: paged decode-step latency and KV-read HBM bandwidth.
+
+Default workload: bs 32, 8192 cached tokens per request, Hq 32 / Hkv 8, head_dim 128,
+page_size 64, bf16 K/V (1.07 GB of KV per step, far larger than the 129 MB L2, so no
+L2 flush is needed between steps).  One step = fused metadata + split-K producer +
+log-sum-exp reducer, replayed from a CUDA graph with PDL.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload NAME]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an independent
+replica of the step on its own GPU (the step has no cross-GPU exchange); the reported
+time is the maximum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-step µs & KV-read HBM GB/s (frac of ~8 TB/s), bs1–64 ctx1K–16K"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "splitk_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="bs32_ctx8k")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the PDL study, e2e and CPU baseline (for profiling runs)")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_metadata_gb300", "csrc")
+    for name in ("pa_splitk.cuh", "pa_common.cuh", "pa_splitk_bf16.cu", "pa_splitk_int8.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per producer launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        rec = json.load(f)
+    entry = rec.get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, f"t_{which}", time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]),
+                                 active=parts[4], hw=parts[5], hw_thermal=parts[6],
+                                 sw_thermal=parts[7], sw_power=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["sm_max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "window": "warm-up tail and timed region"}
+
+
+def oracle_sample_us(wl, tokens, request):
+    """Oracle wall time (us) for one request's first `tokens` cached tokens, all heads."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    meta = oracle.build_metadata(wl.req_pool_indices.numpy(), wl.seq_lens.numpy(),
+                                 wl.req_to_token.numpy(), wl.spec.seqlen_offset,
+                                 wl.max_seq_pages, wl.spec.page_size)
+    if wl.spec.kv_dtype == "int8":
+        k, v, ks, vs = wl.k_cache.numpy(), wl.v_cache.numpy(), wl.k_scale.numpy(), wl.v_scale.numpy()
+    else:
+        k, v, ks, vs = bits(wl.k_cache), bits(wl.v_cache), None, None
+    n = min(tokens, int(meta["cache_seqlens"][request]))
+    q = bits(wl.q)[request:request + 1]
+    t0 = time.perf_counter()
+    oracle.paged_attention(q, k, v, meta["page_table"][request:request + 1],
+                           np.array([n], np.int32), wl.sm_scale, ks, vs)
+    return (time.perf_counter() - t0) * 1e6, n
+
+
+def cpu_baseline(wl, budget_s=12.0, tokens=1024):
+    """Oracle on a bounded sample, scaled to one full step (cost is linear in tokens)."""
+    total_tokens = sum(wl.ctx)
+    spent, sampled, used = 0.0, 0, 0
+    req = 0
+    while spent < budget_s * 1e6 and used < 64:
+        us, n = oracle_sample_us(wl, tokens, req % wl.spec.bs)
+        spent += us
+        sampled += n
+        used += 1
+        req += 1
+    per_step_us = spent / sampled * total_tokens
+    return {"value": per_step_us, "unit": "us/step", "cores": 1, "kind": "oracle",
+            "sample": f"{used} requests x first {tokens} cached tokens, all "
+                      f"{wl.spec.num_q_heads} query heads ({sampled} tokens, {spent / 1e6:.1f} s); "
+                      f"scaled by {total_tokens} tokens per step"}
+
+
+def run_reference(args, spec, rank, world):
+    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    from paged_kv_decode_metadata_gb300 import synthetic
+
+    wl = synthetic.make(spec)
+    tokens = 256
+    for i in range(args.warmup):
+        oracle_sample_us(wl, tokens, i % spec.bs)
+    per_token = []
+    for i in range(args.steps):
+        us, n = oracle_sample_us(wl, tokens, i % spec.bs)
+        per_token.append(us / n)
+    per_step_us = statistics.mean(per_token) * sum(wl.ctx)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": per_step_us, "unit": "us/step",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step_us / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(spec, wl, None),
+        "cpu_baseline": {"value": per_step_us, "unit": "us/step", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: first {tokens} cached tokens of one request, all "
+                                   f"{spec.num_q_heads} query heads; scaled by {sum(wl.ctx)} "
+                                   "tokens per step"},
+        "e2e": {"value": per_step_us, "unit": "us/step", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(spec, wl, num_splits):
+    cfg = {"workload": spec.name, "bs": spec.bs,
+           "ctx": spec.ctx if spec.ragged is None else f"U[{spec.ragged[0]},{spec.ragged[1]}]",
+           "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+           "head_dim": spec.head_dim, "page_size": spec.page_size, "kv_dtype": spec.kv_dtype,
+           "seqlen_offset": spec.seqlen_offset}
+    if num_splits is not None:
+        cfg["num_splits"] = num_splits
+    if spec.swa_window is not None:
+        cfg["swa_window"] = spec.swa_window
+    return cfg
+
+
+def time_graph(torch, graph, n, stream):
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(n):
+            graph.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / n * 1e3  # us
+
+
+def capture(torch, fn, stream):
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return graph
+
+
+def pdl_study(torch, synthetic, DeviceStep, stream, replays=3000):
+    """Graph-replay and eager latency with and without PDL at batch 1."""
+    out = {}
+    for name in ("bs1_ctx1k", "bs1_ctx8k"):
+        wl = synthetic.make(synthetic.WORKLOADS[name])
+        ds = DeviceStep(wl)
+        row = {}
+        for pdl in (False, True):
+            g = capture(torch, lambda: ds.step(use_pdl=pdl), stream)
+            for _ in range(3):
+                time_graph(torch, g, 200, stream)
+            row["graph_pdl_us" if pdl else "graph_us"] = min(
+                time_graph(torch, g, replays, stream) for _ in range(3))
+            del g
+            with torch.cuda.stream(stream):
+                for _ in range(50):
+                    ds.step(use_pdl=pdl)
+                start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                start.record(stream)
+                for _ in range(500):
+                    ds.step(use_pdl=pdl)
+                end.record(stream)
+            end.synchronize()
+            row["eager_pdl_us" if pdl else "eager_us"] = start.elapsed_time(end) / 500 * 1e3
+        row["num_splits"] = ds.num_splits
+        out[name] = row
+        del ds
+    return out
+
+
+def run_gb300(args, spec, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_decode_metadata_gb300 import binding, synthetic
+    from paged_kv_decode_metadata_gb300 import build as pa_build
+    from paged_kv_decode_metadata_gb300.runtime import DeviceStep
+
+    if rank == 0:
+        pa_build.build()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.set_device(local_rank)
+    binding.load()
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+
+    wl = synthetic.make(spec)
+    ds = DeviceStep(wl)
+    stream = torch.cuda.Stream()
+    binding.pa_read_error_flags(reset=True)
+    graph = capture(torch, lambda: ds.step(use_pdl=True), stream)
+    if binding.pa_read_error_flags(reset=True):
+        raise RuntimeError("device error flags set during warm-up")
+
+    sampler = ClockSampler(local_rank)
+    if rank == 0:
+        sampler.start()
+        time.sleep(1.0)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    # keep the GPU busy for ~1.5 s so the clock samples see the loaded state
+    t_end = time.time() + 1.5
+    while time.time() < t_end:
+        for _ in range(200):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps ------------------------------------------------
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark("start")
+    us_step = time_graph(torch, graph, args.steps, stream)
+    torch.cuda.synchronize()
+    sampler.mark("stop")
+    if world > 1:
+        dist.barrier()
+        t = torch.tensor([us_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        us_step = float(t.item())
+    clocks = sampler.stop() if rank == 0 else None
+
+    # ---- dominant kernel alone: the split-K producer, CUDA events on its stream -------
+    n_kernel = max(20, min(args.steps, 500))
+    with torch.cuda.stream(stream):
+        ds.metadata(use_pdl=False)
+        for _ in range(5):
+            ds.splitk(use_pdl=False)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(n_kernel):
+            ds.splitk(use_pdl=False)
+        end.record(stream)
+    end.synchronize()
+    splitk_us = start.elapsed_time(end) / n_kernel * 1e3
+
+    kv_bytes = ds.kv_bytes(wl.ctx)
+    rows = spec.bs * spec.num_q_heads
+    # KV (+ int8 scales) read, Q read, partials written, page table and lengths read
+    splitk_bytes = (kv_bytes + rows * spec.head_dim * 2
+                    + rows * ds.num_splits * (spec.head_dim + 2) * 4
+                    + spec.bs * (4 + wl.max_seq_pages * 4))
+    achieved = splitk_bytes / (splitk_us * 1e-6) / 1e9
+    traffic = ncu_traffic(spec.name)
+    step_bytes = ds.step_bytes(wl.ctx)
+
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        # ---- end to end through the public C ABI with host buffers --------------------
+        pin = dict(pin_memory=True)
+        h_q = wl.q.clone().pin_memory()
+        h_sl = wl.seq_lens.clone().pin_memory()
+        h_rpi = wl.req_pool_indices.clone().pin_memory()
+        h_out = torch.empty(ds.out.shape, dtype=ds.out.dtype, **pin)
+        h_lse = torch.empty(ds.lse.shape, dtype=ds.lse.dtype, **pin)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                ds.q.copy_(h_q, non_blocking=True)
+                ds.seq_lens.copy_(h_sl, non_blocking=True)
+                ds.req_pool_indices.copy_(h_rpi, non_blocking=True)
+                ds.step(use_pdl=True, stream=stream)
+                h_out.copy_(ds.out, non_blocking=True)
+                h_lse.copy_(ds.lse, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(20):
+            e2e_step()
+        n_e2e = max(20, min(args.steps, 2000))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        e2e_us = (time.perf_counter() - t0) / n_e2e * 1e6
+        h2d = h_q.numel() * 2 + h_sl.numel() * 8 + h_rpi.numel() * 8
+        d2h = h_out.numel() * 2 + h_lse.numel() * 4
+        extras["e2e"] = {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
+                         "d2h_bytes_per_step": d2h}
+        # ---- same graph without PDL, and the batch-1 PDL study -------------------------
+        g_nopdl = capture(torch, lambda: ds.step(use_pdl=False), stream)
+        extras["graph_no_pdl_us"] = time_graph(torch, g_nopdl, min(args.steps, 2000), stream)
+        del g_nopdl
+        extras["pdl_bs1"] = pdl_study(torch, synthetic, DeviceStep, stream)
+        extras["cpu_baseline"] = cpu_baseline(wl)
+
+    flags = binding.pa_read_error_flags(reset=True)
+    if flags:
+        raise RuntimeError(f"device error flags 0x{flags:x}")
+    if rank != 0:
+        return
+    kv_gbs = kv_bytes / (us_step * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": us_step, "unit": "us/step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_step / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if spec.kv_dtype == "bf16" else "int8", "data": "synthetic",
+        "config": dict(workload_config(spec, wl, ds.num_splits), pdl=True, cuda_graph=True,
+                       l2="inputs larger than L2: %.2f GB of KV per step, no flush" % (kv_bytes / 1e9),
+                       parallelism="replicas" if world > 1 else "single GPU"),
+        "kv_hbm_gbs": kv_gbs, "kv_hbm_frac": kv_gbs / hbm_peak,
+        "step_hbm_gbs": step_bytes / (us_step * 1e-6) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "splitk_kernel", "achieved": achieved,
+                     "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": splitk_bytes, "launch_us": splitk_us},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    line.update({k: v for k, v in extras.items() if k not in ("cpu_baseline",)})
+    line["cpu_baseline"] = extras.get("cpu_baseline")
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    from paged_kv_decode_metadata_gb300 import synthetic
+
+    spec = synthetic.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, spec, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_gb300(args, spec, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) decode-step paged-KV attention library.
+ *
+ * One decode step runs three kernels chained with Programmatic Dependent Launch:
+ *
+ *   pa_build_metadata  -> pa_decode_splitk  -> pa_reduce
+ *   (fused metadata)      (split-K producer)   (log-sum-exp reducer)
+ *
+ * pa_decode_step issues all three.  Every entry point takes plain device pointers
+ * and sizes, enqueues work on `stream` (a cudaStream_t passed as void*, NULL = the
+ * legacy default stream) and returns without synchronising.  No entry point
+ * allocates memory: the caller owns every buffer, including the split-K scratch.
+ * All launches are capturable into a CUDA graph.  When use_pdl is non-zero the
+ * kernel is launched with the programmatic-stream-serialisation attribute, so it
+ * may start while the previous kernel in the stream finishes; each kernel waits
+ * (griddepcontrol.wait) before it reads anything an earlier kernel wrote.
+ *
+ * Errors.  Arguments are checked on the host before any launch:
+ *   PA_ERR_INVALID      a required pointer is NULL, a size is negative, a stride is
+ *                       smaller than the width it must hold, a pointer is not
+ *                       16-byte aligned where stated, or the workspace is too small;
+ *   PA_ERR_UNSUPPORTED  a shape this build has no kernel for (see each function);
+ *   PA_ERR_CUDA         the launch itself failed (cudaGetLastError after launch).
+ * bs == 0 returns PA_OK and launches nothing.  Values that only the device can see
+ * (a page index outside the pool, a pool row outside req_to_token, a token slot
+ * outside full_to_swa_mapping, a cache length beyond the page table) never cause an
+ * out-of-bounds access: the kernel substitutes a safe index, the affected outputs
+ * are unspecified, and a bit is set in a device-side error word that
+ * pa_read_error_flags returns.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = 1,
+  PA_ERR_UNSUPPORTED = 2,
+  PA_ERR_CUDA = 3
+} pa_status;
+
+typedef enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1 } pa_kv_dtype;
+
+/* Bits of the device-side error word (pa_read_error_flags). */
+#define PA_DEVERR_PAGE_OUT_OF_RANGE 0x1u     /* page_table entry outside [0, num_pages) */
+#define PA_DEVERR_POOL_ROW_OUT_OF_RANGE 0x2u /* req_pool_indices entry outside req_to_token */
+#define PA_DEVERR_SLOT_OUT_OF_RANGE 0x4u     /* token slot outside full_to_swa_mapping */
+#define PA_DEVERR_WAIT_TIMEOUT 0x8u          /* a shared-memory copy wait gave up (~2 s) */
+#define PA_DEVERR_SEQLEN_OUT_OF_RANGE 0x10u  /* cache_seqlens < 0 or > max_seq_pages*page_size */
+
+/* cu_seqlens_q modes of pa_build_metadata_full. */
+#define PA_Q_MODE_NONE 0    /* leave cu_seqlens_q untouched (decode, target-verify) */
+#define PA_Q_MODE_CUMSUM 1  /* cu_seqlens_q[0] = 0, [i+1] = sum_{j<=i} int32(qlens[j]) */
+#define PA_Q_MODE_STRIDED 2 /* cu_seqlens_q[0] = 0, [i+1] = (i+1) * q_stride */
+
+/*
+ * pa_build_metadata -- the fused per-step metadata update.
+ *
+ * Follows sglang "trtllm_mha_graph_metadata.py" (module docstring; kernel
+ * update_trtllm_mha_graph_metadata_kernel and its launcher), which replaces about
+ * 25 small host-dispatched ops per graph replay with one launch:
+ *
+ *   cache_seqlens[i] = int32(seq_lens[i] + seqlen_offset)
+ *   cu_seqlens_k[0]  = 0;  cu_seqlens_k[i+1] = cu_seqlens_k[i] + cache_seqlens[i]
+ *                      (int32, wrapping)
+ *   page_table[i,p]  = req_to_token[req_pool_indices[i], p*page_size] / page_size
+ *                      for 0 <= p < max_seq_pages (C truncating division)
+ *   swa_page_table[i,p] (when full_to_swa_mapping != NULL):
+ *                      t = the same req_to_token entry;
+ *                      s = t >= 0 ? full_to_swa_mapping[t] : -1;
+ *                      s < 0 ? -1 : int32(s / page_size)
+ *
+ * Arguments (all device pointers, row-major):
+ *   req_pool_indices [bs] int64     pool row of each request
+ *   seq_lens         [bs] int64
+ *   req_to_token     [req_to_token_rows, req_to_token_stride] int32 token slots
+ *   full_to_swa_mapping [full_to_swa_mapping_len] int64 or NULL (no sliding window)
+ *   cache_seqlens    [bs] int32 (out)
+ *   cu_seqlens_k     [bs+1] int32 (out; entry 0 is written as 0)
+ *   page_table       [bs, page_table_stride] int32 (out; columns >= max_seq_pages
+ *                    are not touched)
+ *   swa_page_table   [bs, swa_page_table_stride] int32 (out) -- NULL iff the
+ *                    mapping is NULL
+ *   page_size >= 1, max_seq_pages >= 0, (max_seq_pages-1)*page_size <
+ *   req_to_token_stride when max_seq_pages > 0.
+ * Errors: PA_ERR_INVALID as listed in the file comment.
+ */
+pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_t* seq_lens,
+                            const int32_t* req_to_token, int64_t req_to_token_rows,
+                            int64_t req_to_token_stride,
+                            const int64_t* full_to_swa_mapping,
+                            int64_t full_to_swa_mapping_len, int32_t* cache_seqlens,
+                            int32_t* cu_seqlens_k, int32_t* page_table,
+                            int64_t page_table_stride, int32_t* swa_page_table,
+                            int64_t swa_page_table_stride, int32_t bs,
+                            int32_t seqlen_offset, int32_t max_seq_pages,
+                            int32_t page_size, void* stream, int32_t use_pdl);
+
+/*
+ * pa_build_metadata_full -- pa_build_metadata plus the optional outputs of the same
+ * module: cu_seqlens_q in the three modes above (qlens [bs] int64 device pointer for
+ * PA_Q_MODE_CUMSUM, cu_seqlens_q [bs+1] int32 for modes 1 and 2), and the
+ * sliding-window translation of the step's output slots:
+ *   for idx < swa_out_len:  idx < num_out_tokens -> loc = out_cache_loc[idx];
+ *                                                   loc < 0 ? -1 : full_to_swa_mapping[loc]
+ *                           otherwise            -> 0
+ *   num_out_tokens = min(swa_out_len, out_cache_loc_len)
+ * swa_out_cache_loc [swa_out_len] int64 (out) or NULL; it needs the mapping.
+ */
+pa_status pa_build_metadata_full(
+    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
+    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    const int64_t* out_cache_loc, int64_t out_cache_loc_len, const int64_t* qlens,
+    int32_t* cache_seqlens, int32_t* cu_seqlens_k, int32_t* cu_seqlens_q,
+    int32_t* page_table, int64_t page_table_stride, int32_t* swa_page_table,
+    int64_t swa_page_table_stride, int64_t* swa_out_cache_loc, int64_t swa_out_len,
+    int32_t bs, int32_t seqlen_offset, int32_t max_seq_pages, int32_t page_size,
+    int32_t q_mode, int32_t q_stride, void* stream, int32_t use_pdl);
+
+/*
+ * pa_decode_splitk -- the split-K paged-attention producer.
+ *
+ * lmdeploy PR #4861 "perf(cuda): use PDL for paged attention and V4 prefill"
+ * (Changes: Split-K paged attention) names the producer that writes per-split
+ * partials to scratch, signals its dependents before its final scratch stores, and
+ * the reducer that waits immediately before reading them.  The attention is the
+ * plain definition: for request b, query head h and kv head h / (Hq/Hkv), over the
+ * tokens j < cache_seqlens[b] (token j lives in page page_table[b, j/page_size] at
+ * row j % page_size),  x_j = sm_scale * q . K_j.
+ *
+ * Split s of request b covers token positions [s*L, min((s+1)*L, cache_seqlens[b]))
+ * with L = page_size * ceil(max_seq_pages / num_splits) (one split length for the
+ * whole batch, page aligned).  For every (b, h, s) it writes
+ *   scratch_m   = max_j x_j                     (-inf for an empty split)
+ *   scratch_l   = sum_j exp(x_j - scratch_m)    (0 for an empty split)
+ *   scratch_acc = sum_j exp(x_j - scratch_m) V_j (not written for an empty split)
+ *
+ * Layouts (device pointers):
+ *   q            [bs, num_q_heads, head_dim] bf16, 16-byte aligned
+ *   k_cache, v_cache [num_pages, num_kv_heads, page_size, head_dim], bf16
+ *                (PA_KV_BF16) or int8 codes (PA_KV_INT8), 16-byte aligned
+ *   k_scale, v_scale [num_pages, num_kv_heads, page_size] fp32, 16-byte aligned;
+ *                INT8 only (K = k_scale * code, V = v_scale * code); NULL for BF16
+ *   page_table   [bs, page_table_stride] int32; cache_seqlens [bs] int32
+ *   scratch_m, scratch_l [bs, num_q_heads, num_splits] fp32
+ *   scratch_acc  [bs, num_q_heads, num_splits, head_dim] fp32
+ * Supported: head_dim 128; page_size 16, 32, 64, 128; num_q_heads/num_kv_heads in
+ * {1, 2, 4, 8}; otherwise PA_ERR_UNSUPPORTED.
+ */
+pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
+                           const float* k_scale, const float* v_scale, int32_t kv_dtype,
+                           const int32_t* page_table, int64_t page_table_stride,
+                           const int32_t* cache_seqlens, int32_t bs, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                           int64_t num_pages, int32_t max_seq_pages, int32_t num_splits,
+                           float sm_scale, float* scratch_m, float* scratch_l,
+                           float* scratch_acc, void* stream, int32_t use_pdl);
+
+/*
+ * pa_reduce -- the log-sum-exp reducer (the standard and quantized reducer paths of
+ * lmdeploy PR #4861 read the same fp32 partials, so one reducer serves both KV types):
+ *   M = max_s m_s;  L = sum_s l_s exp(m_s - M)
+ *   out[b,h,:] = bf16_rne( sum_s acc_s exp(m_s - M) / L )
+ *   lse[b,h]   = M + ln L   (natural log of the sum of exp of the scaled scores)
+ * Splits with m_s = -inf are skipped without reading their acc.  A request with no
+ * tokens gives out = 0 and lse = -inf.
+ *   out [bs, num_q_heads, head_dim] bf16; lse [bs, num_q_heads] fp32 or NULL.
+ * Supported: head_dim 128.
+ */
+pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const float* scratch_acc,
+                    int32_t bs, int32_t num_q_heads, int32_t head_dim, int32_t num_splits,
+                    void* out, float* lse, void* stream, int32_t use_pdl);
+
+/*
+ * pa_decode_step -- metadata, producer and reducer in one call (three launches; the
+ * second and third carry the PDL attribute when use_pdl is non-zero, the first
+ * too, and it waits before writing anything).  Arguments are those of the three
+ * functions above.  The split-K scratch is carved from `workspace`
+ * (workspace_bytes >= pa_workspace_bytes(bs, num_q_heads, head_dim, S)), where S is
+ * num_splits, or pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, 0)
+ * when num_splits == 0.
+ */
+pa_status pa_decode_step(
+    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
+    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const void* q,
+    const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale,
+    int32_t kv_dtype, int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t num_splits,
+    float sm_scale, void* workspace, size_t workspace_bytes, void* out, float* lse,
+    void* stream, int32_t use_pdl);
+
+/* Bytes of workspace pa_decode_step needs: m, l and acc partials, each 256-byte aligned. */
+size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim,
+                          int32_t num_splits);
+
+/*
+ * Split count heuristic: enough (request, kv head, split) blocks for several waves
+ * of the GPU's SMs, a page-aligned split length, and no split count that leaves the
+ * longest request with an empty split.  sm_count <= 0 queries the current device.
+ * Returns >= 1 (1 for degenerate sizes).
+ */
+int32_t pa_choose_splits(int32_t bs, int32_t num_kv_heads, int32_t max_seq_pages,
+                         int32_t page_size, int32_t sm_count);
+
+/* Static description of a status code. */
+const char* pa_status_string(pa_status status);
+
+/*
+ * Read (and, when reset != 0, clear) the current device's error word.  This call
+ * synchronises the device; it is for tests and diagnostics, not the hot path.
+ */
+pa_status pa_read_error_flags(uint32_t* flags, int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,263 @@
+"""Python binding of the C ABI in include/pa.h (argument marshalling only).
+
+Each function here has the name of the C entry point it calls, takes torch tensors,
+checks that they are CUDA tensors of the expected dtype and layout, and passes their
+device pointers through ctypes.  All arithmetic runs in the library's kernels; there
+is no fallback: if ``_build/libpa.so`` is missing the first call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
+PA_KV_BF16, PA_KV_INT8 = 0, 1
+PA_Q_MODE_NONE, PA_Q_MODE_CUMSUM, PA_Q_MODE_STRIDED = 0, 1, 2
+DEVERR_PAGE_OUT_OF_RANGE = 0x1
+DEVERR_POOL_ROW_OUT_OF_RANGE = 0x2
+DEVERR_SLOT_OUT_OF_RANGE = 0x4
+DEVERR_WAIT_TIMEOUT = 0x8
+DEVERR_SEQLEN_OUT_OF_RANGE = 0x10
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        self.status = status
+        super().__init__(f"{func} failed: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libpa.so (built by ``build.build()``); raise if it is not there."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is missing; build it with "
+                    "`python -m paged_kv_decode_metadata_gb300.build`")
+            _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def _declare(lib):
+    vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t)
+    lib.pa_build_metadata.argtypes = [vp, vp, vp, i64, i64, vp, i64, vp, vp, vp, i64, vp, i64,
+                                      i32, i32, i32, i32, vp, i32]
+    lib.pa_build_metadata_full.argtypes = [vp, vp, vp, i64, i64, vp, i64, vp, i64, vp, vp, vp,
+                                           vp, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32,
+                                           i32, i32, vp, i32]
+    lib.pa_decode_splitk.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, i32, i32, i32, i32,
+                                     i32, i64, i32, i32, f32, vp, vp, vp, vp, i32]
+    lib.pa_reduce.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32]
+    lib.pa_decode_step.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp, vp, vp, i64,
+                                   vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                   i64, i32, f32, vp, sz, vp, vp, vp, i32]
+    lib.pa_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.pa_workspace_bytes.restype = sz
+    lib.pa_choose_splits.argtypes = [i32, i32, i32, i32, i32]
+    lib.pa_choose_splits.restype = i32
+    lib.pa_status_string.argtypes = [i32]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_read_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    for name in ("pa_build_metadata", "pa_build_metadata_full", "pa_decode_splitk", "pa_reduce",
+                 "pa_decode_step", "pa_read_error_flags"):
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().pa_status_string(int(status)).decode()
+
+
+def _check(func: str, status: int):
+    if status != PA_OK:
+        raise PAError(func, status)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _row_stride(t: torch.Tensor, name: str) -> int:
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be 2-D with unit column stride")
+    return t.stride(0)
+
+
+def _ptr2d(t: torch.Tensor, dtype, name: str) -> int:
+    """Pointer of a row-strided 2-D CUDA tensor (rows may be padded)."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    _row_stride(t, name)
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def pa_build_metadata(req_pool_indices, seq_lens, req_to_token, cache_seqlens, cu_seqlens_k,
+                      page_table, *, seqlen_offset: int, max_seq_pages: int, page_size: int,
+                      full_to_swa_mapping=None, swa_page_table=None, stream=None,
+                      use_pdl: bool = True):
+    """Fused metadata update; see include/pa.h.  Outputs are written in place."""
+    return pa_build_metadata_full(req_pool_indices, seq_lens, req_to_token, cache_seqlens,
+                                  cu_seqlens_k, page_table, seqlen_offset=seqlen_offset,
+                                  max_seq_pages=max_seq_pages, page_size=page_size,
+                                  full_to_swa_mapping=full_to_swa_mapping,
+                                  swa_page_table=swa_page_table, stream=stream, use_pdl=use_pdl)
+
+
+def pa_build_metadata_full(req_pool_indices, seq_lens, req_to_token, cache_seqlens,
+                           cu_seqlens_k, page_table, *, seqlen_offset: int, max_seq_pages: int,
+                           page_size: int, full_to_swa_mapping=None, swa_page_table=None,
+                           cu_seqlens_q=None, qlens=None, q_mode: int = PA_Q_MODE_NONE,
+                           q_stride: int = 0, out_cache_loc=None, swa_out_cache_loc=None,
+                           stream=None, use_pdl: bool = True):
+    lib = load()
+    bs = req_pool_indices.shape[0]
+    pt_stride = _row_stride(page_table, "page_table")
+    swa_stride = _row_stride(swa_page_table, "swa_page_table") if swa_page_table is not None else 0
+    st = lib.pa_build_metadata_full(
+        _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
+        _ptr(seq_lens, torch.int64, "seq_lens"),
+        _ptr2d(req_to_token, torch.int32, "req_to_token"),
+        req_to_token.shape[0], req_to_token.stride(0),
+        _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
+        full_to_swa_mapping.numel() if full_to_swa_mapping is not None else 0,
+        _ptr(out_cache_loc, torch.int64, "out_cache_loc"),
+        out_cache_loc.numel() if out_cache_loc is not None else 0,
+        _ptr(qlens, torch.int64, "qlens"),
+        _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
+        _ptr(cu_seqlens_k, torch.int32, "cu_seqlens_k"),
+        _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q"),
+        _ptr2d(page_table, torch.int32, "page_table"), pt_stride,
+        _ptr2d(swa_page_table, torch.int32, "swa_page_table") if swa_page_table is not None else None,
+        swa_stride,
+        _ptr(swa_out_cache_loc, torch.int64, "swa_out_cache_loc"),
+        swa_out_cache_loc.numel() if swa_out_cache_loc is not None else 0,
+        bs, int(seqlen_offset), int(max_seq_pages), int(page_size), int(q_mode), int(q_stride),
+        _stream(stream), int(bool(use_pdl)))
+    _check("pa_build_metadata_full", st)
+
+
+def _kv_args(k_cache, v_cache, k_scale, v_scale):
+    if k_cache.dtype == torch.bfloat16:
+        return PA_KV_BF16, None, None
+    if k_cache.dtype == torch.int8:
+        if k_scale is None or v_scale is None:
+            raise ValueError("int8 KV needs k_scale and v_scale")
+        return PA_KV_INT8, _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale")
+    raise ValueError(f"unsupported KV dtype {k_cache.dtype}")
+
+
+def pa_decode_splitk(q, k_cache, v_cache, page_table, cache_seqlens, scratch_m, scratch_l,
+                     scratch_acc, *, max_seq_pages: int, num_splits: int, sm_scale: float,
+                     k_scale=None, v_scale=None, stream=None, use_pdl: bool = True):
+    """Split-K producer: writes per-split (m, l, acc) partials; see include/pa.h."""
+    lib = load()
+    kv_dtype, ks, vs = _kv_args(k_cache, v_cache, k_scale, v_scale)
+    bs, hq, d = q.shape
+    num_pages, hkv, page_size, _ = k_cache.shape
+    st = lib.pa_decode_splitk(
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
+        ks, vs, kv_dtype, _ptr2d(page_table, torch.int32, "page_table"),
+        _row_stride(page_table, "page_table"),
+        _ptr(cache_seqlens, torch.int32, "cache_seqlens"), bs, hq, hkv, d, page_size, num_pages,
+        int(max_seq_pages), int(num_splits), float(sm_scale),
+        _ptr(scratch_m, torch.float32, "scratch_m"), _ptr(scratch_l, torch.float32, "scratch_l"),
+        _ptr(scratch_acc, torch.float32, "scratch_acc"), _stream(stream), int(bool(use_pdl)))
+    _check("pa_decode_splitk", st)
+
+
+def pa_reduce(scratch_m, scratch_l, scratch_acc, out, lse=None, *, stream=None,
+              use_pdl: bool = True):
+    """Log-sum-exp reducer: writes out (bf16) and lse (fp32); see include/pa.h."""
+    lib = load()
+    bs, hq, s = scratch_m.shape
+    d = scratch_acc.shape[-1]
+    st = lib.pa_reduce(_ptr(scratch_m, torch.float32, "scratch_m"),
+                       _ptr(scratch_l, torch.float32, "scratch_l"),
+                       _ptr(scratch_acc, torch.float32, "scratch_acc"), bs, hq, d, s,
+                       _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+                       _stream(stream), int(bool(use_pdl)))
+    _check("pa_reduce", st)
+
+
+def pa_decode_step(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: int,
+                   max_seq_pages: int, cache_seqlens, cu_seqlens_k, page_table, q, k_cache,
+                   v_cache, num_splits: int, sm_scale: float, workspace, out, lse=None,
+                   k_scale=None, v_scale=None, full_to_swa_mapping=None, swa_page_table=None,
+                   stream=None, use_pdl: bool = True):
+    """Metadata + split-K producer + reducer in one call; see include/pa.h."""
+    lib = load()
+    kv_dtype, ks, vs = _kv_args(k_cache, v_cache, k_scale, v_scale)
+    bs, hq, d = q.shape
+    num_pages, hkv, page_size, _ = k_cache.shape
+    st = lib.pa_decode_step(
+        _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
+        _ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
+        req_to_token.shape[0], req_to_token.stride(0),
+        _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
+        full_to_swa_mapping.numel() if full_to_swa_mapping is not None else 0,
+        int(seqlen_offset), int(max_seq_pages), _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
+        _ptr(cu_seqlens_k, torch.int32, "cu_seqlens_k"), _ptr2d(page_table, torch.int32, "page_table"),
+        _row_stride(page_table, "page_table"),
+        _ptr2d(swa_page_table, torch.int32, "swa_page_table") if swa_page_table is not None else None,
+        _row_stride(swa_page_table, "swa_page_table") if swa_page_table is not None else 0,
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"),
+        _ptr(v_cache, None, "v_cache"), ks, vs, kv_dtype, bs, hq, hkv, d, page_size, num_pages,
+        int(num_splits), float(sm_scale), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _ptr(out, torch.bfloat16, "out"),
+        _ptr(lse, torch.float32, "lse"), _stream(stream), int(bool(use_pdl)))
+    _check("pa_decode_step", st)
+
+
+def pa_workspace_bytes(bs: int, num_q_heads: int, head_dim: int, num_splits: int) -> int:
+    return int(load().pa_workspace_bytes(bs, num_q_heads, head_dim, num_splits))
+
+
+def pa_choose_splits(bs: int, num_kv_heads: int, max_seq_pages: int, page_size: int,
+                     sm_count: int = 0) -> int:
+    return int(load().pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, sm_count))
+
+
+def pa_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def pa_read_error_flags(reset: bool = True) -> int:
+    """Device error word (synchronises the device); see include/pa.h."""
+    v = ctypes.c_uint32(0)
+    _check("pa_read_error_flags", load().pa_read_error_flags(ctypes.byref(v), int(bool(reset))))
+    return int(v.value)

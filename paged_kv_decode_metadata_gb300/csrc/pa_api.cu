@@ -1,0 +1,372 @@
+// C ABI of the decode-step library: argument checks, split heuristic, workspace
+// layout and the three-launch decode step.  See include/pa.h for the contract.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+// Device-side error word.  Kernels receive its device address; host code fetches
+// that address once per device with cudaGetSymbolAddress.
+__device__ unsigned int g_pa_error_flags;
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned int*> g_err_ptr[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
+
+cudaError_t error_word(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned int* p = g_err_ptr[dev].load();
+  if (p == nullptr) {
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_pa_error_flags);
+    if (e != cudaSuccess) return e;
+    p = static_cast<unsigned int*>(addr);
+    g_err_ptr[dev].store(p);
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
+int sm_count_of_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = g_sm_count[dev].load();
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev].store(n);
+  }
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+pa_status check_metadata(const int64_t* req_pool_indices, const int64_t* seq_lens,
+                         const int32_t* req_to_token, int64_t req_to_token_rows,
+                         int64_t req_to_token_stride, const int64_t* mapping,
+                         int64_t mapping_len, int32_t* cache_seqlens, int32_t* cu_seqlens_k,
+                         int32_t* page_table, int64_t page_table_stride,
+                         int32_t* swa_page_table, int64_t swa_page_table_stride, int32_t bs,
+                         int32_t max_seq_pages, int32_t page_size) {
+  if (bs < 0 || max_seq_pages < 0 || page_size < 1) return PA_ERR_INVALID;
+  if (bs == 0) return PA_OK;
+  if (!req_pool_indices || !seq_lens || !cache_seqlens || !cu_seqlens_k || !page_table)
+    return PA_ERR_INVALID;
+  if (bs >= (1 << 30)) return PA_ERR_INVALID;
+  if (page_table_stride < max_seq_pages) return PA_ERR_INVALID;
+  if (max_seq_pages > 0) {
+    if (!req_to_token || req_to_token_rows < 1) return PA_ERR_INVALID;
+    if (static_cast<int64_t>(max_seq_pages - 1) * page_size >= req_to_token_stride)
+      return PA_ERR_INVALID;
+  }
+  if ((mapping == nullptr) != (swa_page_table == nullptr)) return PA_ERR_INVALID;
+  if (mapping != nullptr) {
+    if (mapping_len < 1 || swa_page_table_stride < max_seq_pages) return PA_ERR_INVALID;
+  }
+  return PA_OK;
+}
+
+pa_status check_attention(const void* q, const void* k_cache, const void* v_cache,
+                          const float* k_scale, const float* v_scale, int32_t kv_dtype,
+                          const int32_t* page_table, int64_t page_table_stride,
+                          const int32_t* cache_seqlens, int32_t bs, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                          int64_t num_pages, int32_t max_seq_pages, int32_t num_splits) {
+  if (bs < 0) return PA_ERR_INVALID;
+  if (bs == 0) return PA_OK;
+  if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_INT8) return PA_ERR_INVALID;
+  if (!q || !k_cache || !v_cache || !page_table || !cache_seqlens) return PA_ERR_INVALID;
+  if (kv_dtype == PA_KV_INT8 && (!k_scale || !v_scale)) return PA_ERR_INVALID;
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
+    return PA_ERR_INVALID;
+  if (num_pages < 1 || max_seq_pages < 1 || page_table_stride < max_seq_pages)
+    return PA_ERR_INVALID;
+  if (num_splits < 1 || num_splits > 4096) return PA_ERR_INVALID;
+  if (bs > 65535 || num_kv_heads > 65535) return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID;
+  if (kv_dtype == PA_KV_INT8 && (!aligned16(k_scale) || !aligned16(v_scale)))
+    return PA_ERR_INVALID;
+  const int group = num_q_heads / num_kv_heads;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
+    return PA_ERR_UNSUPPORTED;
+  if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_seq_pages) * page_size > INT32_MAX) return PA_ERR_INVALID;
+  return PA_OK;
+}
+
+pa_status launch_metadata_checked(const pa::MetadataParams& p, cudaStream_t stream,
+                                  int32_t use_pdl) {
+  cudaError_t e = pa::launch_metadata(p, stream, use_pdl != 0);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_build_metadata_full(
+    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
+    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    const int64_t* out_cache_loc, int64_t out_cache_loc_len, const int64_t* qlens,
+    int32_t* cache_seqlens, int32_t* cu_seqlens_k, int32_t* cu_seqlens_q,
+    int32_t* page_table, int64_t page_table_stride, int32_t* swa_page_table,
+    int64_t swa_page_table_stride, int64_t* swa_out_cache_loc, int64_t swa_out_len,
+    int32_t bs, int32_t seqlen_offset, int32_t max_seq_pages, int32_t page_size,
+    int32_t q_mode, int32_t q_stride, void* stream, int32_t use_pdl) {
+  pa_status st = check_metadata(req_pool_indices, seq_lens, req_to_token, req_to_token_rows,
+                                req_to_token_stride, full_to_swa_mapping,
+                                full_to_swa_mapping_len, cache_seqlens, cu_seqlens_k,
+                                page_table, page_table_stride, swa_page_table,
+                                swa_page_table_stride, bs, max_seq_pages, page_size);
+  if (st != PA_OK || bs == 0) return st;
+  if (q_mode < 0 || q_mode > 2) return PA_ERR_INVALID;
+  if (q_mode != 0 && cu_seqlens_q == nullptr) return PA_ERR_INVALID;
+  if (q_mode == 1 && qlens == nullptr) return PA_ERR_INVALID;
+  if (swa_out_cache_loc != nullptr) {
+    if (full_to_swa_mapping == nullptr || swa_out_len < 0 || out_cache_loc_len < 0)
+      return PA_ERR_INVALID;
+    if (out_cache_loc_len > 0 && out_cache_loc == nullptr) return PA_ERR_INVALID;
+    if (cdiv(swa_out_len, 256) > (1 << 30)) return PA_ERR_INVALID;
+  }
+  pa::MetadataParams p = {};
+  p.req_pool_indices = req_pool_indices;
+  p.seq_lens = seq_lens;
+  p.req_to_token = req_to_token;
+  p.req_to_token_rows = req_to_token_rows;
+  p.req_to_token_stride = req_to_token_stride;
+  p.full_to_swa_mapping = full_to_swa_mapping;
+  p.mapping_len = full_to_swa_mapping_len;
+  p.out_cache_loc = out_cache_loc;
+  p.num_out_tokens = swa_out_cache_loc != nullptr
+                         ? (out_cache_loc_len < swa_out_len ? out_cache_loc_len : swa_out_len)
+                         : 0;
+  p.qlens = qlens;
+  p.cache_seqlens = cache_seqlens;
+  p.cu_seqlens_k = cu_seqlens_k;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.page_table = page_table;
+  p.page_table_stride = page_table_stride;
+  p.swa_page_table = swa_page_table;
+  p.swa_page_table_stride = swa_page_table_stride;
+  p.swa_out_cache_loc = swa_out_cache_loc;
+  p.swa_out_len = swa_out_cache_loc != nullptr ? swa_out_len : 0;
+  p.bs = bs;
+  p.seqlen_offset = seqlen_offset;
+  p.max_seq_pages = max_seq_pages;
+  p.page_size = page_size;
+  p.q_mode = q_mode;
+  p.q_stride = q_stride;
+  cudaError_t e = error_word(&p.err);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  return launch_metadata_checked(p, static_cast<cudaStream_t>(stream), use_pdl);
+}
+
+pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_t* seq_lens,
+                            const int32_t* req_to_token, int64_t req_to_token_rows,
+                            int64_t req_to_token_stride,
+                            const int64_t* full_to_swa_mapping,
+                            int64_t full_to_swa_mapping_len, int32_t* cache_seqlens,
+                            int32_t* cu_seqlens_k, int32_t* page_table,
+                            int64_t page_table_stride, int32_t* swa_page_table,
+                            int64_t swa_page_table_stride, int32_t bs,
+                            int32_t seqlen_offset, int32_t max_seq_pages,
+                            int32_t page_size, void* stream, int32_t use_pdl) {
+  return pa_build_metadata_full(
+      req_pool_indices, seq_lens, req_to_token, req_to_token_rows, req_to_token_stride,
+      full_to_swa_mapping, full_to_swa_mapping_len, nullptr, 0, nullptr, cache_seqlens,
+      cu_seqlens_k, nullptr, page_table, page_table_stride, swa_page_table,
+      swa_page_table_stride, nullptr, 0, bs, seqlen_offset, max_seq_pages, page_size,
+      PA_Q_MODE_NONE, 0, stream, use_pdl);
+}
+
+pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
+                           const float* k_scale, const float* v_scale, int32_t kv_dtype,
+                           const int32_t* page_table, int64_t page_table_stride,
+                           const int32_t* cache_seqlens, int32_t bs, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                           int64_t num_pages, int32_t max_seq_pages, int32_t num_splits,
+                           float sm_scale, float* scratch_m, float* scratch_l,
+                           float* scratch_acc, void* stream, int32_t use_pdl) {
+  pa_status st = check_attention(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
+                                 page_table_stride, cache_seqlens, bs, num_q_heads,
+                                 num_kv_heads, head_dim, page_size, num_pages, max_seq_pages,
+                                 num_splits);
+  if (st != PA_OK || bs == 0) return st;
+  if (!scratch_m || !scratch_l || !scratch_acc || !aligned16(scratch_acc))
+    return PA_ERR_INVALID;
+  pa::SplitKParams p = {};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.page_table = page_table;
+  p.page_table_stride = page_table_stride;
+  p.cache_seqlens = cache_seqlens;
+  p.num_pages = num_pages;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.max_seq_pages = max_seq_pages;
+  p.pages_per_split = static_cast<int32_t>(cdiv(max_seq_pages, num_splits));
+  p.num_splits = num_splits;
+  p.q_scale = sm_scale * 1.4426950408889634f;  // log2(e): the kernel works in base 2
+  p.m_out = scratch_m;
+  p.l_out = scratch_l;
+  p.acc_out = scratch_acc;
+  cudaError_t e = error_word(&p.err);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  const int group = num_q_heads / num_kv_heads;
+  e = kv_dtype == PA_KV_INT8
+          ? pa::launch_splitk_int8(p, bs, group, page_size, static_cast<cudaStream_t>(stream),
+                                   use_pdl != 0)
+          : pa::launch_splitk_bf16(p, bs, group, page_size, static_cast<cudaStream_t>(stream),
+                                   use_pdl != 0);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return from_cuda(e);
+}
+
+pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const float* scratch_acc,
+                    int32_t bs, int32_t num_q_heads, int32_t head_dim, int32_t num_splits,
+                    void* out, float* lse, void* stream, int32_t use_pdl) {
+  if (bs < 0 || num_q_heads < 1 || num_splits < 1 || num_splits > 4096) return PA_ERR_INVALID;
+  if (bs == 0) return PA_OK;
+  if (!scratch_m || !scratch_l || !scratch_acc || !out) return PA_ERR_INVALID;
+  if (!aligned16(scratch_acc) || (reinterpret_cast<uintptr_t>(out) & 7u) != 0)
+    return PA_ERR_INVALID;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  pa::ReduceParams p = {};
+  p.m = scratch_m;
+  p.l = scratch_l;
+  p.acc = scratch_acc;
+  p.num_rows = static_cast<int64_t>(bs) * num_q_heads;
+  p.num_splits = num_splits;
+  p.out = out;
+  p.lse = lse;
+  cudaError_t e = pa::launch_reduce(p, static_cast<cudaStream_t>(stream), use_pdl != 0);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return from_cuda(e);
+}
+
+size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim,
+                          int32_t num_splits) {
+  if (bs <= 0 || num_q_heads <= 0 || head_dim <= 0 || num_splits <= 0) return 0;
+  const size_t rows = static_cast<size_t>(bs) * num_q_heads * num_splits;
+  return 2 * align256(rows * sizeof(float)) + align256(rows * head_dim * sizeof(float));
+}
+
+int32_t pa_choose_splits(int32_t bs, int32_t num_kv_heads, int32_t max_seq_pages,
+                         int32_t page_size, int32_t sm_count) {
+  if (bs <= 0 || num_kv_heads <= 0 || max_seq_pages <= 0 || page_size <= 0) return 1;
+  if (sm_count <= 0) sm_count = sm_count_of_current_device();
+  if (sm_count <= 0) sm_count = 152;
+  // Aim for about eight waves of two resident blocks per SM, so the block scheduler
+  // can balance ragged requests and the last wave is a small fraction of the step.
+  const int64_t units = static_cast<int64_t>(bs) * num_kv_heads;
+  const int64_t target_blocks = static_cast<int64_t>(sm_count) * 2 * 8;
+  int64_t want = cdiv(target_blocks, units);
+  // At least two 64-token chunks per split keep the per-block prologue amortised.
+  const int64_t chunks = cdiv(static_cast<int64_t>(max_seq_pages) * page_size, 64);
+  const int64_t most = chunks / 2 > 0 ? chunks / 2 : 1;
+  if (want > most) want = most;
+  if (want < 1) want = 1;
+  if (want > 4096) want = 4096;
+  // Equal page-aligned split length; drop splits the longest request would leave empty.
+  const int64_t pages_per_split = cdiv(max_seq_pages, want);
+  return static_cast<int32_t>(cdiv(max_seq_pages, pages_per_split));
+}
+
+pa_status pa_decode_step(
+    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
+    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const void* q,
+    const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale,
+    int32_t kv_dtype, int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t num_splits,
+    float sm_scale, void* workspace, size_t workspace_bytes, void* out, float* lse,
+    void* stream, int32_t use_pdl) {
+  if (bs < 0) return PA_ERR_INVALID;
+  if (bs == 0) return PA_OK;
+  if (num_splits < 0) return PA_ERR_INVALID;
+  const int32_t splits =
+      num_splits > 0 ? num_splits
+                     : pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, 0);
+  pa_status st = check_metadata(req_pool_indices, seq_lens, req_to_token, req_to_token_rows,
+                                req_to_token_stride, full_to_swa_mapping,
+                                full_to_swa_mapping_len, cache_seqlens, cu_seqlens_k,
+                                page_table, page_table_stride, swa_page_table,
+                                swa_page_table_stride, bs, max_seq_pages, page_size);
+  if (st != PA_OK) return st;
+  st = check_attention(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
+                       page_table_stride, cache_seqlens, bs, num_q_heads, num_kv_heads,
+                       head_dim, page_size, num_pages, max_seq_pages, splits);
+  if (st != PA_OK) return st;
+  if (!out || !workspace || !aligned16(workspace)) return PA_ERR_INVALID;
+  if (workspace_bytes < pa_workspace_bytes(bs, num_q_heads, head_dim, splits))
+    return PA_ERR_INVALID;
+  const size_t rows = static_cast<size_t>(bs) * num_q_heads * splits;
+  char* ws = static_cast<char*>(workspace);
+  float* m = reinterpret_cast<float*>(ws);
+  float* l = reinterpret_cast<float*>(ws + align256(rows * sizeof(float)));
+  float* acc = reinterpret_cast<float*>(ws + 2 * align256(rows * sizeof(float)));
+
+  st = pa_build_metadata(req_pool_indices, seq_lens, req_to_token, req_to_token_rows,
+                         req_to_token_stride, full_to_swa_mapping, full_to_swa_mapping_len,
+                         cache_seqlens, cu_seqlens_k, page_table, page_table_stride,
+                         swa_page_table, swa_page_table_stride, bs, seqlen_offset,
+                         max_seq_pages, page_size, stream, use_pdl);
+  if (st != PA_OK) return st;
+  st = pa_decode_splitk(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
+                        page_table_stride, cache_seqlens, bs, num_q_heads, num_kv_heads,
+                        head_dim, page_size, num_pages, max_seq_pages, splits, sm_scale, m, l,
+                        acc, stream, use_pdl);
+  if (st != PA_OK) return st;
+  return pa_reduce(m, l, acc, bs, num_q_heads, head_dim, splits, out, lse, stream, use_pdl);
+}
+
+const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape";
+    case PA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+pa_status pa_read_error_flags(uint32_t* flags, int32_t reset) {
+  if (flags == nullptr) return PA_ERR_INVALID;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_pa_error_flags, sizeof(v));
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  *flags = v;
+  if (reset) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_pa_error_flags, &zero, sizeof(zero));
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// Host-side interface between the C ABI (pa_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct MetadataParams {
+  const int64_t* req_pool_indices;
+  const int64_t* seq_lens;
+  const int32_t* req_to_token;
+  int64_t req_to_token_rows;
+  int64_t req_to_token_stride;
+  const int64_t* full_to_swa_mapping;  // nullptr: no sliding-window outputs
+  int64_t mapping_len;
+  const int64_t* out_cache_loc;
+  int64_t num_out_tokens;  // valid prefix of out_cache_loc (already min'ed)
+  const int64_t* qlens;
+  int32_t* cache_seqlens;
+  int32_t* cu_seqlens_k;
+  int32_t* cu_seqlens_q;
+  int32_t* page_table;
+  int64_t page_table_stride;
+  int32_t* swa_page_table;
+  int64_t swa_page_table_stride;
+  int64_t* swa_out_cache_loc;
+  int64_t swa_out_len;
+  int32_t bs;
+  int32_t seqlen_offset;
+  int32_t max_seq_pages;
+  int32_t page_size;
+  int32_t q_mode;
+  int32_t q_stride;
+  unsigned int* err;
+};
+
+struct SplitKParams {
+  const void* q;  // bf16 [bs, Hq, 128]
+  const void* k_cache;
+  const void* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* page_table;
+  int64_t page_table_stride;
+  const int32_t* cache_seqlens;
+  int64_t num_pages;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t max_seq_pages;
+  int32_t pages_per_split;
+  int32_t num_splits;
+  float q_scale;  // sm_scale * log2(e)
+  float* m_out;
+  float* l_out;
+  float* acc_out;
+  unsigned int* err;
+};
+
+struct ReduceParams {
+  const float* m;
+  const float* l;
+  const float* acc;
+  int64_t num_rows;  // bs * Hq
+  int32_t num_splits;
+  void* out;   // bf16 [num_rows, 128]
+  float* lse;  // [num_rows] or nullptr
+};
+
+cudaError_t launch_metadata(const MetadataParams& p, cudaStream_t stream, bool use_pdl);
+
+// bs, grid and shapes are validated by the caller.
+cudaError_t launch_splitk_bf16(const SplitKParams& p, int bs, int group, int page_size,
+                               cudaStream_t stream, bool use_pdl);
+cudaError_t launch_splitk_int8(const SplitKParams& p, int bs, int group, int page_size,
+                               cudaStream_t stream, bool use_pdl);
+
+cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool use_pdl);
+
+}  // namespace pa

@@ -1,0 +1,161 @@
+// Fused decode-step metadata update, one launch per step.
+//
+// Semantics: sglang "trtllm_mha_graph_metadata.py" (module docstring and the kernel
+// update_trtllm_mha_graph_metadata_kernel): cache_seqlens, the int32 cu_seqlens_k
+// scan, the page_table gather from req_to_token, the optional sliding-window page
+// table through full_to_swa_mapping with the -1 sentinel, the optional cu_seqlens_q
+// modes and the optional swa_out_cache_loc translation.
+//
+// Grid: blocks [0, bs) each own one request row (its cache_seqlens entry and its
+// page-table row(s)); block bs runs the in-block scans; blocks after it translate
+// swa_out_cache_loc in tiles of kThreads entries.  Every block waits on the previous
+// grid before its first global access (so a PDL launch never overwrites a page
+// table that a previous step's producer may still read) and triggers its dependents
+// straight after: the producer reads nothing this kernel reads, and its own
+// griddepcontrol.wait blocks until this grid has completed and flushed.
+#include <utility>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Block-wide inclusive scan of one uint32 per thread (wrapping adds).  Returns the
+// thread's inclusive prefix; *total receives the block total.
+__device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_sums,
+                                                         uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t up = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += up;
+  }
+  if (lane == 31) warp_sums[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < kThreads / 32 ? warp_sums[lane] : 0u;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t up = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += up;
+    }
+    if (lane < kThreads / 32) warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const uint32_t before = warp > 0 ? warp_sums[warp - 1] : 0u;
+  *total = warp_sums[kThreads / 32 - 1];
+  __syncthreads();  // warp_sums is reused by the next call
+  return v + before;
+}
+
+__global__ void __launch_bounds__(kThreads) metadata_kernel(const MetadataParams p) {
+  grid_dependency_wait();
+  trigger_dependents();
+
+  const int tid = threadIdx.x;
+  const int blk = blockIdx.x;
+
+  if (blk < p.bs) {
+    // ---- one request row -------------------------------------------------------
+    const int i = blk;
+    int64_t row = p.req_pool_indices[i];
+    const bool row_ok = row >= 0 && row < p.req_to_token_rows;
+    if (!row_ok) {
+      if (tid == 0) record_error(p.err, kErrPoolRowOutOfRange);
+      row = 0;
+    }
+    if (tid == 0) {
+      const uint64_t sum = static_cast<uint64_t>(p.seq_lens[i]) +
+                           static_cast<uint64_t>(static_cast<int64_t>(p.seqlen_offset));
+      p.cache_seqlens[i] = static_cast<int32_t>(static_cast<uint32_t>(sum));
+    }
+    const int32_t* row_in = p.req_to_token + row * p.req_to_token_stride;
+    int32_t* row_out = p.page_table + static_cast<int64_t>(i) * p.page_table_stride;
+    int32_t* swa_out = p.swa_page_table != nullptr
+                           ? p.swa_page_table + static_cast<int64_t>(i) * p.swa_page_table_stride
+                           : nullptr;
+    for (int col = tid; col < p.max_seq_pages; col += kThreads) {
+      const int32_t token = row_ok ? row_in[static_cast<int64_t>(col) * p.page_size] : 0;
+      row_out[col] = token / p.page_size;
+      if (swa_out != nullptr) {
+        int64_t swa_token = -1;
+        if (token >= 0) {
+          if (token < p.mapping_len) {
+            swa_token = p.full_to_swa_mapping[token];
+          } else {
+            record_error(p.err, kErrSlotOutOfRange);
+          }
+        }
+        swa_out[col] = swa_token < 0 ? -1 : static_cast<int32_t>(swa_token / p.page_size);
+      }
+    }
+    return;
+  }
+
+  if (blk == p.bs) {
+    // ---- scans: cu_seqlens_k, and cu_seqlens_q in the computed modes -------------
+    __shared__ uint32_t warp_sums[kThreads / 32];
+    uint32_t carry = 0;
+    for (int base = 0; base < p.bs; base += kThreads) {
+      const int j = base + tid;
+      const uint32_t v = j < p.bs ? static_cast<uint32_t>(p.seq_lens[j]) +
+                                        static_cast<uint32_t>(p.seqlen_offset)
+                                  : 0u;
+      uint32_t total;
+      const uint32_t incl = block_inclusive_scan(v, warp_sums, &total);
+      if (j < p.bs) p.cu_seqlens_k[j + 1] = static_cast<int32_t>(incl + carry);
+      carry += total;
+    }
+    if (tid == 0) p.cu_seqlens_k[0] = 0;
+    if (p.q_mode == 1) {
+      carry = 0;
+      for (int base = 0; base < p.bs; base += kThreads) {
+        const int j = base + tid;
+        const uint32_t v = j < p.bs ? static_cast<uint32_t>(p.qlens[j]) : 0u;
+        uint32_t total;
+        const uint32_t incl = block_inclusive_scan(v, warp_sums, &total);
+        if (j < p.bs) p.cu_seqlens_q[j + 1] = static_cast<int32_t>(incl + carry);
+        carry += total;
+      }
+      if (tid == 0) p.cu_seqlens_q[0] = 0;
+    } else if (p.q_mode == 2) {
+      for (int j = tid; j < p.bs; j += kThreads) {
+        p.cu_seqlens_q[j + 1] =
+            static_cast<int32_t>(static_cast<uint32_t>(j + 1) * static_cast<uint32_t>(p.q_stride));
+      }
+      if (tid == 0) p.cu_seqlens_q[0] = 0;
+    }
+    return;
+  }
+
+  // ---- swa_out_cache_loc tile ------------------------------------------------------
+  const int64_t idx = static_cast<int64_t>(blk - p.bs - 1) * kThreads + tid;
+  if (idx >= p.swa_out_len) return;
+  int64_t value = 0;
+  if (idx < p.num_out_tokens) {
+    const int64_t loc = p.out_cache_loc[idx];
+    if (loc < 0) {
+      value = -1;
+    } else if (loc < p.mapping_len) {
+      value = p.full_to_swa_mapping[loc];
+    } else {
+      record_error(p.err, kErrSlotOutOfRange);
+      value = -1;
+    }
+  }
+  p.swa_out_cache_loc[idx] = value;
+}
+
+}  // namespace
+
+cudaError_t launch_metadata(const MetadataParams& p, cudaStream_t stream, bool use_pdl) {
+  const int64_t out_blocks =
+      p.swa_out_cache_loc != nullptr ? (p.swa_out_len + kThreads - 1) / kThreads : 0;
+  const dim3 grid(static_cast<unsigned>(p.bs + 1 + out_blocks));
+  return launch_kernel(metadata_kernel, grid, dim3(kThreads), 0, stream, use_pdl, p);
+}
+
+}  // namespace pa

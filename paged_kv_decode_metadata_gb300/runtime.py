@@ -1,0 +1,114 @@
+"""Device buffers for one decode step (PyTorch allocates, the library computes).
+
+``DeviceStep`` holds device copies of a workload's inputs, the metadata outputs, the
+split-K scratch and the outputs, and runs the three stages through the C ABI, either
+one by one or as ``pa_decode_step``.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class DeviceStep:
+    def __init__(self, wl, device="cuda", num_splits: int | None = None,
+                 page_table_stride: int | None = None, with_swa: bool = True):
+        spec = wl.spec
+        self.spec = spec
+        self.device = device
+        self.bs = spec.bs
+        self.num_q_heads, self.num_kv_heads = spec.num_q_heads, spec.num_kv_heads
+        self.head_dim, self.page_size = spec.head_dim, spec.page_size
+        self.seqlen_offset = spec.seqlen_offset
+        self.max_seq_pages = wl.max_seq_pages
+        self.sm_scale = wl.sm_scale
+        to = dict(device=device)
+        self.req_pool_indices = wl.req_pool_indices.to(**to)
+        self.seq_lens = wl.seq_lens.to(**to)
+        self.req_to_token = wl.req_to_token.to(**to)
+        self.q = wl.q.to(**to)
+        self.k_cache = wl.k_cache.to(**to)
+        self.v_cache = wl.v_cache.to(**to)
+        self.k_scale = wl.k_scale.to(**to) if wl.k_scale is not None else None
+        self.v_scale = wl.v_scale.to(**to) if wl.v_scale is not None else None
+        self.full_to_swa_mapping = (wl.full_to_swa_mapping.to(**to)
+                                    if with_swa and wl.full_to_swa_mapping is not None else None)
+        if num_splits is None:
+            num_splits = spec.num_splits or B.pa_choose_splits(
+                self.bs, self.num_kv_heads, self.max_seq_pages, self.page_size)
+        self.num_splits = int(num_splits)
+        pts = page_table_stride or self.max_seq_pages
+        i32 = dict(dtype=torch.int32, device=device)
+        self.cache_seqlens = torch.empty(self.bs, **i32)
+        self.cu_seqlens_k = torch.empty(self.bs + 1, **i32)
+        self.page_table = torch.empty((self.bs, pts), **i32)
+        self.swa_page_table = (torch.empty((self.bs, pts), **i32)
+                               if self.full_to_swa_mapping is not None else None)
+        f32 = dict(dtype=torch.float32, device=device)
+        S = self.num_splits
+        self.scratch_m = torch.empty((self.bs, self.num_q_heads, S), **f32)
+        self.scratch_l = torch.empty((self.bs, self.num_q_heads, S), **f32)
+        self.scratch_acc = torch.empty((self.bs, self.num_q_heads, S, self.head_dim), **f32)
+        self.workspace = torch.empty(
+            B.pa_workspace_bytes(self.bs, self.num_q_heads, self.head_dim, S),
+            dtype=torch.uint8, device=device)
+        self.out = torch.empty((self.bs, self.num_q_heads, self.head_dim), dtype=torch.bfloat16,
+                               device=device)
+        self.lse = torch.empty((self.bs, self.num_q_heads), **f32)
+
+    # ---- the three stages ---------------------------------------------------------
+    def metadata(self, use_pdl=True, stream=None):
+        B.pa_build_metadata(self.req_pool_indices, self.seq_lens, self.req_to_token,
+                            self.cache_seqlens, self.cu_seqlens_k, self.page_table,
+                            seqlen_offset=self.seqlen_offset, max_seq_pages=self.max_seq_pages,
+                            page_size=self.page_size, full_to_swa_mapping=self.full_to_swa_mapping,
+                            swa_page_table=self.swa_page_table, stream=stream, use_pdl=use_pdl)
+
+    def splitk(self, use_pdl=True, stream=None):
+        B.pa_decode_splitk(self.q, self.k_cache, self.v_cache, self.page_table,
+                           self.cache_seqlens, self.scratch_m, self.scratch_l, self.scratch_acc,
+                           max_seq_pages=self.max_seq_pages, num_splits=self.num_splits,
+                           sm_scale=self.sm_scale, k_scale=self.k_scale, v_scale=self.v_scale,
+                           stream=stream, use_pdl=use_pdl)
+
+    def reduce(self, use_pdl=True, stream=None):
+        B.pa_reduce(self.scratch_m, self.scratch_l, self.scratch_acc, self.out, self.lse,
+                    stream=stream, use_pdl=use_pdl)
+
+    def stages(self, use_pdl=True, stream=None):
+        self.metadata(use_pdl, stream)
+        self.splitk(use_pdl, stream)
+        self.reduce(use_pdl, stream)
+
+    def step(self, use_pdl=True, stream=None):
+        B.pa_decode_step(req_pool_indices=self.req_pool_indices, seq_lens=self.seq_lens,
+                         req_to_token=self.req_to_token, seqlen_offset=self.seqlen_offset,
+                         max_seq_pages=self.max_seq_pages, cache_seqlens=self.cache_seqlens,
+                         cu_seqlens_k=self.cu_seqlens_k, page_table=self.page_table, q=self.q,
+                         k_cache=self.k_cache, v_cache=self.v_cache, num_splits=self.num_splits,
+                         sm_scale=self.sm_scale, workspace=self.workspace, out=self.out,
+                         lse=self.lse, k_scale=self.k_scale, v_scale=self.v_scale,
+                         full_to_swa_mapping=self.full_to_swa_mapping,
+                         swa_page_table=self.swa_page_table, stream=stream, use_pdl=use_pdl)
+
+    # ---- accounting -----------------------------------------------------------------
+    def kv_bytes(self, ctx) -> int:
+        """Bytes of K and V (plus int8 scales) the step must read: every cached token of
+        every request, for every KV head."""
+        per_token = 2 * self.head_dim * self.k_cache.element_size()
+        if self.k_scale is not None:
+            per_token += 2 * 4
+        return sum(ctx) * self.num_kv_heads * per_token
+
+    def step_bytes(self, ctx) -> int:
+        """Algorithmic HBM bytes of one decode step: KV (+scales), Q read, O and LSE
+        written, split-K scratch written once and read once, and the metadata."""
+        rows = self.bs * self.num_q_heads
+        q_o = rows * self.head_dim * 2 * 2 + rows * 4
+        scratch = 2 * rows * self.num_splits * (self.head_dim + 2) * 4
+        meta = self.bs * (8 + 8 + 4 + 4) + 4 + self.bs * self.max_seq_pages * (4 + 4)
+        if self.swa_page_table is not None:
+            meta += self.bs * self.max_seq_pages * (4 + 8)
+        return self.kv_bytes(ctx) + q_o + scratch + meta

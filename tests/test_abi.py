@@ -1,0 +1,90 @@
+"""The C ABI library loads, exports every function include/pa.h declares, and rejects
+bad arguments on the host (none of these calls reaches the GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_decode_metadata_gb300 import binding as B
+from paged_kv_decode_metadata_gb300 import build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_path_calls():
+    names = declared_functions()
+    for required in ("pa_build_metadata", "pa_decode_splitk", "pa_reduce", "pa_decode_step"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+FAKE = 1 << 20   # an aligned, never-dereferenced device address
+
+
+def _splitk(lib, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, ks=None, vs=None, kv=0, pt=FAKE, pts=16, cl=FAKE, bs=2,
+                hq=32, hkv=8, d=128, P=64, pages=100, msp=16, S=4, scale=0.1, m=FAKE, l=FAKE,
+                acc=FAKE)
+    args.update(over)
+    a = args
+    return lib.pa_decode_splitk(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["kv"], a["pt"], a["pts"],
+                                a["cl"], a["bs"], a["hq"], a["hkv"], a["d"], a["P"], a["pages"],
+                                a["msp"], a["S"], a["scale"], a["m"], a["l"], a["acc"], None, 1)
+
+
+def test_splitk_host_validation(lib):
+    assert _splitk(lib, bs=0) == B.PA_OK                      # empty batch: nothing launched
+    assert _splitk(lib, q=None) == B.PA_ERR_INVALID
+    assert _splitk(lib, hq=30) == B.PA_ERR_INVALID            # not a multiple of Hkv
+    assert _splitk(lib, S=0) == B.PA_ERR_INVALID
+    assert _splitk(lib, pts=8) == B.PA_ERR_INVALID            # stride narrower than the table
+    assert _splitk(lib, q=FAKE + 8) == B.PA_ERR_INVALID       # misaligned
+    assert _splitk(lib, kv=1) == B.PA_ERR_INVALID             # int8 without scales
+    assert _splitk(lib, d=64) == B.PA_ERR_UNSUPPORTED
+    assert _splitk(lib, P=48) == B.PA_ERR_UNSUPPORTED
+    assert _splitk(lib, hq=128) == B.PA_ERR_UNSUPPORTED       # group 16
+
+
+def test_reduce_and_metadata_host_validation(lib):
+    assert lib.pa_reduce(FAKE, FAKE, FAKE, 0, 32, 128, 4, FAKE, None, None, 1) == B.PA_OK
+    assert lib.pa_reduce(None, FAKE, FAKE, 1, 32, 128, 4, FAKE, None, None, 1) == B.PA_ERR_INVALID
+    assert lib.pa_reduce(FAKE, FAKE, FAKE, 1, 32, 64, 4, FAKE, None, None, 1) == B.PA_ERR_UNSUPPORTED
+    md = lambda **o: lib.pa_build_metadata(
+        o.get("rpi", FAKE), FAKE, FAKE, 4, o.get("r2ts", 1024), o.get("map", None), 0, FAKE, FAKE,
+        FAKE, o.get("pts", 16), o.get("swa", None), 16, o.get("bs", 2), 0, 16, 64, None, 1)
+    assert md(bs=0) == B.PA_OK
+    assert md(rpi=None) == B.PA_ERR_INVALID
+    assert md(r2ts=15 * 64) == B.PA_ERR_INVALID               # column 15*64 outside the row
+    assert md(pts=8) == B.PA_ERR_INVALID
+    assert md(map=FAKE) == B.PA_ERR_INVALID                   # mapping without swa output
+    assert md(swa=FAKE) == B.PA_ERR_INVALID                   # swa output without mapping
+
+
+def test_workspace_and_split_heuristic(lib):
+    assert B.pa_workspace_bytes(32, 32, 128, 10) == 2 * 10240 * 4 + 10240 * 128 * 4
+    assert B.pa_workspace_bytes(0, 32, 128, 4) == 0
+    for bs, hkv, pages in ((1, 8, 16), (8, 8, 16), (1, 8, 128), (32, 8, 128), (64, 8, 256), (1, 1, 1)):
+        s = B.pa_choose_splits(bs, hkv, pages, 64, 152)
+        assert 1 <= s <= max(1, pages)
+        pps = -(-pages // s)
+        assert -(-pages // pps) == s          # the longest request has no empty split
+    assert B.pa_choose_splits(0, 8, 16, 64, 152) == 1
+    assert B.pa_status_string(B.PA_ERR_UNSUPPORTED) == "unsupported shape"

@@ -1,0 +1,247 @@
+"""GPU parity of the split-K producer, the reducer and the whole decode step against
+the float64 oracle (O max-abs <= 1e-2, LSE <= 1e-3), plus the properties the CUDA path
+must have exactly: PDL on/off, eager vs CUDA-graph replay, page relabelling."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_metadata_gb300 import binding as B
+from paged_kv_decode_metadata_gb300 import build, synthetic
+from paged_kv_decode_metadata_gb300.runtime import DeviceStep
+
+from helpers import (LSE_ATOL, O_ATOL, assert_attention_close, bits, oracle_attention,
+                     oracle_metadata, oracle_partials)
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    B.load()
+    B.pa_read_error_flags(reset=True)
+    yield
+    _CACHE.clear()
+    torch.cuda.empty_cache()
+
+
+def named(name):
+    if name not in _CACHE:
+        _CACHE.clear()                      # keep at most one large workload resident
+        torch.cuda.empty_cache()
+        wl = synthetic.make(synthetic.WORKLOADS[name])
+        _CACHE[name] = (wl, DeviceStep(wl))
+    return _CACHE[name]
+
+
+def _sample_rows(wl, k):
+    """The longest and shortest requests plus evenly spaced others."""
+    order = np.argsort(wl.ctx)
+    pick = {int(order[0]), int(order[-1])}
+    pick.update(int(x) for x in np.linspace(0, wl.spec.bs - 1, k).round())
+    return np.array(sorted(pick))
+
+
+def _check_flags():
+    assert B.pa_read_error_flags(reset=True) == 0
+
+
+# ---- whole step on the five workloads --------------------------------------------------
+
+@pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER)
+def test_decode_step_matches_oracle(name):
+    wl, ds = named(name)
+    ds.step(use_pdl=True)
+    torch.cuda.synchronize()
+    _check_flags()
+    meta = oracle_metadata(wl)
+    assert np.array_equal(ds.cache_seqlens.cpu().numpy(), meta["cache_seqlens"])
+    assert np.array_equal(ds.page_table.cpu().numpy()[:, :wl.max_seq_pages], meta["page_table"])
+    if ds.swa_page_table is not None:
+        assert np.array_equal(ds.swa_page_table.cpu().numpy(), meta["swa_page_table"])
+    rows = np.arange(wl.spec.bs) if wl.spec.bs <= 8 else _sample_rows(wl, 6)
+    out_ref, lse_ref = oracle_attention(wl, meta, rows)
+    assert_attention_close(ds.out[rows], ds.lse[rows], out_ref, lse_ref, name)
+
+
+@pytest.mark.parametrize("name", ["bs1_ctx1k", "bs8_ctx1k", "bs1_ctx8k"])
+def test_splitk_scratch_matches_oracle_partials(name):
+    wl, ds = named(name)
+    ds.metadata()
+    ds.splitk()
+    torch.cuda.synchronize()
+    _check_flags()
+    meta = oracle_metadata(wl)
+    m_ref, l_ref, acc_ref = oracle_partials(wl, meta, ds.num_splits)
+    m = ds.scratch_m.cpu().numpy().astype(np.float64)
+    l = ds.scratch_l.cpu().numpy().astype(np.float64)
+    acc = ds.scratch_acc.cpu().numpy().astype(np.float64)
+    empty = np.isneginf(m_ref)
+    assert np.array_equal(np.isneginf(m), empty)
+    assert np.all(l[empty] == 0)
+    full = ~empty
+    assert np.abs(m[full] - m_ref[full]).max() <= 1e-4 * max(1.0, np.abs(m_ref[full]).max())
+    assert np.all(np.abs(l[full] - l_ref[full]) <= 1e-4 * l_ref[full])
+    vmax = float(wl.v_cache.float().abs().max())
+    tol = 2e-4 * l_ref[full][:, None] * vmax + 1e-6
+    assert np.all(np.abs(acc[full] - acc_ref[full]) <= tol)
+
+
+def test_reduce_alone_matches_oracle_combine():
+    g = torch.Generator().manual_seed(3)
+    bs, hq, S, d = 3, 8, 37, 128
+    m = torch.randn(bs, hq, S, generator=g, dtype=torch.float64) * 4
+    m[0, 0, :] = -np.inf                      # a row with no tokens
+    m[1, :, ::3] = -np.inf                    # empty splits among full ones
+    l = torch.rand(bs, hq, S, generator=g, dtype=torch.float64) * 50 + 1
+    l[torch.isinf(m)] = 0
+    acc = torch.randn(bs, hq, S, d, generator=g, dtype=torch.float64) * l[..., None]
+    acc[torch.isinf(m)] = float("nan")        # must never be read
+    m32, l32, acc32 = (t.float() for t in (m, l, acc))
+    out = torch.empty(bs, hq, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(bs, hq, dtype=torch.float32, device="cuda")
+    B.pa_reduce(m32.cuda(), l32.cuda(), acc32.cuda(), out, lse)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.combine_splits(m32.double().numpy(), l32.double().numpy(),
+                                           acc32.double().numpy())
+    assert_attention_close(out, lse, o_ref, lse_ref, "reduce")
+
+
+# ---- small random shapes: every group size, page size and KV type ---------------------
+
+SMALL = [(seed, kv, grp, P) for seed, (kv, grp, P) in enumerate(
+    [(kv, grp, P) for kv in ("bf16", "int8") for grp in (1, 2, 4, 8) for P in (16, 32, 64, 128)])]
+
+
+@pytest.mark.parametrize("seed,kv,grp,P", SMALL)
+def test_small_shapes_match_oracle(seed, kv, grp, P):
+    spec = synthetic.small_spec(500 + seed, kv_dtype=kv, group=grp, page_size=P, ctx_max=330)
+    wl = synthetic.make(spec)
+    ds = DeviceStep(wl, page_table_stride=wl.max_seq_pages + 2)
+    ds.step()
+    torch.cuda.synchronize()
+    _check_flags()
+    meta = oracle_metadata(wl)
+    out_ref, lse_ref = oracle_attention(wl, meta)
+    assert_attention_close(ds.out, ds.lse, out_ref, lse_ref, spec.name)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 16, 40])
+def test_split_count_does_not_change_result(splits):
+    spec = synthetic.Spec("splits", bs=3, num_q_heads=16, num_kv_heads=4, num_pages=40,
+                          ragged=(100, 700), num_splits=splits, seed=900)
+    wl = synthetic.make(spec)
+    ds = DeviceStep(wl)
+    ds.step()
+    torch.cuda.synchronize()
+    meta = oracle_metadata(wl)
+    out_ref, lse_ref = oracle_attention(wl, meta)
+    assert_attention_close(ds.out, ds.lse, out_ref, lse_ref, f"S={splits}")
+
+
+def test_empty_and_single_token_requests():
+    spec = synthetic.Spec("edge", bs=4, num_q_heads=8, num_kv_heads=2, num_pages=20,
+                          ragged=(1, 200), num_splits=3, seed=901)
+    wl = synthetic.make(spec)
+    # request 0 attends to nothing, request 1 to a single token
+    wl.seq_lens[0] = -spec.seqlen_offset
+    wl.seq_lens[1] = 1 - spec.seqlen_offset
+    wl.ctx[0], wl.ctx[1] = 0, 1
+    ds = DeviceStep(wl)
+    ds.step()
+    torch.cuda.synchronize()
+    _check_flags()
+    meta = oracle_metadata(wl)
+    out_ref, lse_ref = oracle_attention(wl, meta)
+    assert np.all(np.isneginf(lse_ref[0]))
+    assert_attention_close(ds.out, ds.lse, out_ref, lse_ref, "edge")
+
+
+# ---- exact properties of the CUDA path --------------------------------------------------
+
+def _outputs(ds):
+    return [t.clone() for t in (ds.cache_seqlens, ds.cu_seqlens_k, ds.page_table, ds.out, ds.lse)]
+
+
+@pytest.mark.parametrize("name", ["bs1_ctx8k", "bs64_ragged16k_int8_swa"])
+def test_pdl_on_off_bit_identical(name):
+    wl, ds = named(name)
+    ds.step(use_pdl=True)
+    a = _outputs(ds)
+    ds.out.zero_()
+    ds.step(use_pdl=False)
+    b = _outputs(ds)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.uint8) if x.dtype == torch.bfloat16 else x,
+                           y.view(torch.uint8) if y.dtype == torch.bfloat16 else y)
+
+
+@pytest.mark.parametrize("use_pdl", [True, False])
+def test_graph_replay_bit_identical_to_eager(use_pdl):
+    wl, ds = named("bs8_ctx1k")
+    ds.step(use_pdl=use_pdl)
+    torch.cuda.synchronize()
+    eager = _outputs(ds)
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        ds.step(use_pdl=use_pdl)            # warm up on the capture stream
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        ds.step(use_pdl=use_pdl)
+    ds.out.zero_()
+    ds.lse.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for x, y in zip(eager, _outputs(ds)):
+        assert torch.equal(x, y)
+
+
+def test_page_relabelling_bit_identical_on_gpu():
+    spec = synthetic.Spec("relabel", bs=4, num_q_heads=32, num_kv_heads=8, num_pages=80,
+                          ragged=(300, 1200), num_splits=5, seed=902)
+    wl = synthetic.make(spec)
+    ds = DeviceStep(wl)
+    ds.step()
+    out1, lse1 = ds.out.clone(), ds.lse.clone()
+    perm = torch.randperm(spec.num_pages, generator=torch.Generator().manual_seed(1))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(spec.num_pages)
+    wl2 = synthetic.make(spec)
+    wl2.k_cache = wl.k_cache[perm].contiguous()
+    wl2.v_cache = wl.v_cache[perm].contiguous()
+    P = spec.page_size
+    r2t = wl.req_to_token.clone()
+    for i in range(spec.bs):
+        n = wl.ctx[i]
+        t = r2t[int(wl.req_pool_indices[i]), :n]
+        r2t[int(wl.req_pool_indices[i]), :n] = inv[(t // P).long()].to(torch.int32) * P + t % P
+    wl2.req_to_token = r2t
+    ds2 = DeviceStep(wl2)
+    ds2.step()
+    torch.cuda.synchronize()
+    assert torch.equal(out1, ds2.out) and torch.equal(lse1, ds2.lse)
+
+
+def test_out_of_range_page_sets_error_flag_without_fault():
+    spec = synthetic.Spec("badpage", bs=2, num_q_heads=8, num_kv_heads=2, num_pages=12,
+                          ctx=200, num_splits=2, seed=903)
+    wl = synthetic.make(spec)
+    ds = DeviceStep(wl)
+    ds.metadata()
+    ds.page_table[1, 2] = spec.num_pages + 5   # a page the pool does not have
+    B.pa_read_error_flags(reset=True)
+    ds.splitk()
+    ds.reduce()
+    flags = B.pa_read_error_flags(reset=True)
+    assert flags & B.DEVERR_PAGE_OUT_OF_RANGE
+    # request 0 is unaffected
+    meta = oracle_metadata(wl)
+    out_ref, lse_ref = oracle_attention(wl, meta, [0])
+    assert_attention_close(ds.out[:1], ds.lse[:1], out_ref, lse_ref, "request 0")
