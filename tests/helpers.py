@@ -8,9 +8,22 @@ import torch
 import oracle
 
 # Tolerances of the attention outputs against the float64 oracle: bf16 output max-abs
-# error 1e-2, natural-log LSE max-abs error 1e-3.
+# error 1e-2, natural-log LSE max-abs error 1e-3.  bf16 keeps 8 significant bits, so
+# for |out| >= 4 half a bf16 ulp (2^-6 and up) alone exceeds 1e-2 and no bf16 output
+# can meet a flat 1e-2 there.  Where half an ulp of the reference value plus 2e-3 is
+# larger than 1e-2, that is the bound instead (only |out| >= 4 is affected).
 O_ATOL = 1e-2
 LSE_ATOL = 1e-3
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |x| (normal range)."""
+    _, e = np.frexp(np.abs(x))            # |x| = m * 2**e, m in [0.5, 1)
+    return np.ldexp(1.0, e - 8)
+
+
+def out_tolerance(ref: np.ndarray) -> np.ndarray:
+    return np.maximum(O_ATOL, 0.5 * bf16_ulp(ref) + 2e-3)
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
@@ -58,6 +71,7 @@ def assert_attention_close(out_gpu, lse_gpu, out_ref, lse_ref, what=""):
     full = ~empty
     o_err = np.abs(o[full] - out_ref[full]).max() if full.any() else 0.0
     l_err = np.abs(lse[full] - lse_ref[full]).max() if full.any() else 0.0
-    assert o_err <= O_ATOL, f"{what}: out max abs err {o_err}"
+    excess = (np.abs(o[full] - out_ref[full]) - out_tolerance(out_ref[full])).max() if full.any() else 0.0
+    assert excess <= 0, f"{what}: out max abs err {o_err} beyond tolerance by {excess}"
     assert l_err <= LSE_ATOL, f"{what}: lse max abs err {l_err}"
     return o_err, l_err
