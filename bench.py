@@ -40,7 +40,9 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="bs32_ctx8k")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the PDL study, e2e and CPU baseline (for profiling runs)")
+                    help="skip the PDL study, e2e and CPU baseline")
+    ap.add_argument("--profile", action="store_true",
+                    help="eager steps only (warm-up + steps launches of each kernel), for ncu")
     return ap.parse_args()
 
 
@@ -157,22 +159,21 @@ def oracle_sample_us(wl, tokens, request):
     return (time.perf_counter() - t0) * 1e6, n
 
 
-def cpu_baseline(wl, budget_s=12.0, tokens=1024):
-    """Oracle on a bounded sample, scaled to one full step (cost is linear in tokens)."""
+def cpu_baseline(wl, budget_s=10.0):
+    """The oracle on whole requests of the workload (all cached tokens, all heads), one
+    request after another until ~budget_s of CPU time; scaled to one full step."""
     total_tokens = sum(wl.ctx)
     spent, sampled, used = 0.0, 0, 0
-    req = 0
-    while spent < budget_s * 1e6 and used < 64:
-        us, n = oracle_sample_us(wl, tokens, req % wl.spec.bs)
+    while spent < budget_s * 1e6 and used < 4 * wl.spec.bs:
+        us, n = oracle_sample_us(wl, 1 << 30, used % wl.spec.bs)
         spent += us
         sampled += n
         used += 1
-        req += 1
     per_step_us = spent / sampled * total_tokens
     return {"value": per_step_us, "unit": "us/step", "cores": 1, "kind": "oracle",
-            "sample": f"{used} requests x first {tokens} cached tokens, all "
-                      f"{wl.spec.num_q_heads} query heads ({sampled} tokens, {spent / 1e6:.1f} s); "
-                      f"scaled by {total_tokens} tokens per step"}
+            "sample": f"{used} whole requests ({sampled} cached tokens x "
+                      f"{wl.spec.num_q_heads} query heads, {spent / 1e6:.1f} s on one core); "
+                      f"scaled to the step's {total_tokens} tokens"}
 
 
 def run_reference(args, spec, rank, world):
@@ -414,6 +415,29 @@ def run_gb300(args, spec, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args, spec):
+    """Plain eager decode steps with no timing, sampling or extras: the command that
+    ncu captures.  Kernel launch order per step: metadata, split-K producer, reducer."""
+    import torch
+
+    from paged_kv_decode_metadata_gb300 import binding, synthetic
+    from paged_kv_decode_metadata_gb300 import build as pa_build
+    from paged_kv_decode_metadata_gb300.runtime import DeviceStep
+
+    pa_build.build()
+    binding.load()
+    wl = synthetic.make(spec)
+    ds = DeviceStep(wl)
+    for _ in range(args.warmup + args.steps):
+        ds.step(use_pdl=True)
+    torch.cuda.synchronize()
+    flags = binding.pa_read_error_flags(reset=True)
+    if flags:
+        raise RuntimeError(f"device error flags 0x{flags:x}")
+    print(json.dumps({"profile": spec.name, "steps": args.warmup + args.steps,
+                      "num_splits": ds.num_splits}))
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -424,6 +448,9 @@ def main():
     spec = synthetic.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, spec, rank, world)
+        return
+    if args.profile:
+        run_profile(args, spec)
         return
     if world > 1:
         import torch
