@@ -42,7 +42,9 @@ typedef enum {
   PA_OK = 0,
   PA_ERR_INVALID = 1,
   PA_ERR_UNSUPPORTED = 2,
-  PA_ERR_CUDA = 3
+  PA_ERR_CUDA = 3,
+  PA_ERR_SCRATCH_LIMIT = 4 /* pa_decode_step_static_scratch: step needs more scratch
+                              than PA_STATIC_SCRATCH_BYTES */
 } pa_status;
 
 typedef enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1 } pa_kv_dtype;
@@ -199,6 +201,42 @@ pa_status pa_decode_step(
     int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t num_splits,
     float sm_scale, void* workspace, size_t workspace_bytes, void* out, float* lse,
     void* stream, int32_t use_pdl);
+
+/*
+ * pa_decode_step_static_scratch -- pa_decode_step for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this call; it is an addition of
+ * this library.
+ *
+ * Some callers cannot call cudaMalloc where they run a decode step: code running while
+ * a CUDA graph is being captured (cudaMalloc synchronises the device, which capture
+ * forbids), runtimes whose device memory is owned entirely by their own allocator or
+ * fixed at start-up, and plain C hosts with no allocator of their own.  This call
+ * takes the same arguments as pa_decode_step except the workspace: the split-K
+ * scratch comes from an array of PA_STATIC_SCRATCH_BYTES compiled into the library.
+ * Inputs and outputs are still the caller's.
+ *   - Every GPU that loads the library holds that array until the process exits.
+ *   - A step whose scratch, pa_workspace_bytes(bs, num_q_heads, head_dim, S), exceeds
+ *     PA_STATIC_SCRATCH_BYTES returns PA_ERR_SCRATCH_LIMIT and launches nothing.
+ *   - The first call on a device looks up the array's device address; make it before
+ *     any stream capture.
+ *   - All calls share the array and it keeps the last call's contents (nothing in it
+ *     needs to start at zero).  Calls whose work overlaps on the GPU race on it: keep
+ *     them in order on one stream.
+ *   - It allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ */
+#define PA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+pa_status pa_decode_step_static_scratch(
+    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
+    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const void* q,
+    const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale,
+    int32_t kv_dtype, int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t num_splits,
+    float sm_scale, void* out, float* lse, void* stream, int32_t use_pdl);
 
 /* Bytes of workspace pa_decode_step needs: m, l and acc partials, each 256-byte aligned. */
 size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim,

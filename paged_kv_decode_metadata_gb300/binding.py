@@ -17,7 +17,8 @@ import torch
 
 from . import build as _build
 
-PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_SCRATCH_LIMIT = 0, 1, 2, 3, 4
+PA_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 PA_KV_BF16, PA_KV_INT8 = 0, 1
 PA_Q_MODE_NONE, PA_Q_MODE_CUMSUM, PA_Q_MODE_STRIDED = 0, 1, 2
 DEVERR_PAGE_OUT_OF_RANGE = 0x1
@@ -68,6 +69,11 @@ def _declare(lib):
     lib.pa_decode_step.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp, vp, vp, i64,
                                    vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                    i64, i32, f32, vp, sz, vp, vp, vp, i32]
+    lib.pa_decode_step_static_scratch.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp,
+                                                  vp, vp, i64, vp, i64, vp, vp, vp, vp, vp, i32,
+                                                  i32, i32, i32, i32, i32, i64, i32, f32, vp, vp,
+                                                  vp, i32]
+    lib.pa_decode_step_static_scratch.restype = ctypes.c_int
     lib.pa_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.pa_workspace_bytes.restype = sz
     lib.pa_choose_splits.argtypes = [i32, i32, i32, i32, i32]
@@ -241,6 +247,37 @@ def pa_decode_step(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: i
         workspace.numel() * workspace.element_size(), _ptr(out, torch.bfloat16, "out"),
         _ptr(lse, torch.float32, "lse"), _stream(stream), int(bool(use_pdl)))
     _check("pa_decode_step", st)
+
+
+def pa_decode_step_static_scratch(*, req_pool_indices, seq_lens, req_to_token,
+                                  seqlen_offset: int, max_seq_pages: int, cache_seqlens,
+                                  cu_seqlens_k, page_table, q, k_cache, v_cache,
+                                  num_splits: int, sm_scale: float, out, lse=None, k_scale=None,
+                                  v_scale=None, full_to_swa_mapping=None, swa_page_table=None,
+                                  stream=None, use_pdl: bool = True):
+    """pa_decode_step without a workspace argument, for callers that cannot allocate:
+    the split-K scratch is the library's built-in array (see include/pa.h).  Calls
+    share that array, so calls must not overlap on the GPU."""
+    lib = load()
+    kv_dtype, ks, vs = _kv_args(k_cache, v_cache, k_scale, v_scale)
+    bs, hq, d = q.shape
+    num_pages, hkv, page_size, _ = k_cache.shape
+    st = lib.pa_decode_step_static_scratch(
+        _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
+        _ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
+        req_to_token.shape[0], req_to_token.stride(0),
+        _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
+        full_to_swa_mapping.numel() if full_to_swa_mapping is not None else 0,
+        int(seqlen_offset), int(max_seq_pages), _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
+        _ptr(cu_seqlens_k, torch.int32, "cu_seqlens_k"), _ptr2d(page_table, torch.int32, "page_table"),
+        _row_stride(page_table, "page_table"),
+        _ptr2d(swa_page_table, torch.int32, "swa_page_table") if swa_page_table is not None else None,
+        _row_stride(swa_page_table, "swa_page_table") if swa_page_table is not None else 0,
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"),
+        _ptr(v_cache, None, "v_cache"), ks, vs, kv_dtype, bs, hq, hkv, d, page_size, num_pages,
+        int(num_splits), float(sm_scale), _ptr(out, torch.bfloat16, "out"),
+        _ptr(lse, torch.float32, "lse"), _stream(stream), int(bool(use_pdl)))
+    _check("pa_decode_step_static_scratch", st)
 
 
 def pa_workspace_bytes(bs: int, num_q_heads: int, head_dim: int, num_splits: int) -> int:

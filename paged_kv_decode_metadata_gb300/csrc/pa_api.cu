@@ -349,6 +349,7 @@ const char* pa_status_string(pa_status status) {
     case PA_ERR_INVALID: return "invalid argument";
     case PA_ERR_UNSUPPORTED: return "unsupported shape";
     case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_SCRATCH_LIMIT: return "step needs more scratch than the static array holds";
   }
   return "unknown status";
 }
