@@ -57,7 +57,8 @@ def measured_peaks():
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_metadata_gb300", "csrc")
-    for name in ("pa_splitk.cuh", "pa_common.cuh", "pa_splitk_bf16.cu", "pa_splitk_int8.cu"):
+    for name in ("pa_splitk_mma.cuh", "pa_common.cuh", "pa_splitk_mma_bf16.cu",
+                 "pa_splitk_mma_int8.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -327,17 +328,25 @@ def run_gb300(args, spec, rank, world, local_rank):
 
     # ---- dominant kernel alone: the split-K producer, CUDA events on its stream -------
     n_kernel = max(20, min(args.steps, 500))
-    with torch.cuda.stream(stream):
-        ds.metadata(use_pdl=False)
-        for _ in range(5):
-            ds.splitk(use_pdl=False)
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(n_kernel):
-            ds.splitk(use_pdl=False)
-        end.record(stream)
-    end.synchronize()
-    splitk_us = start.elapsed_time(end) / n_kernel * 1e3
+
+    def producer_us():
+        with torch.cuda.stream(stream):
+            ds.metadata(use_pdl=False)
+            for _ in range(5):
+                ds.splitk(use_pdl=False)
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for _ in range(n_kernel):
+                ds.splitk(use_pdl=False)
+            end.record(stream)
+        end.synchronize()
+        return start.elapsed_time(end) / n_kernel * 1e3
+
+    splitk_us = producer_us()
+    producer_alt = {}
+    if spec.num_q_heads // spec.num_kv_heads <= 8:
+        with binding.producer(binding.PA_PRODUCER_FMA):
+            producer_alt["fma_us"] = producer_us()
 
     kv_bytes = ds.kv_bytes(wl.ctx)
     rows = spec.bs * spec.num_q_heads
@@ -403,7 +412,8 @@ def run_gb300(args, spec, rank, world, local_rank):
                        parallelism="replicas" if world > 1 else "single GPU"),
         "kv_hbm_gbs": kv_gbs, "kv_hbm_frac": kv_gbs / hbm_peak,
         "step_hbm_gbs": step_bytes / (us_step * 1e-6) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "splitk_kernel", "achieved": achieved,
+        "producer_cuda_core_fma_us": producer_alt.get("fma_us"),
+        "roofline": {"bound": "hbm", "kernel": "splitk_mma_kernel", "achieved": achieved,
                      "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": splitk_bytes, "launch_us": splitk_us},

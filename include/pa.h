@@ -49,6 +49,13 @@ typedef enum {
 
 typedef enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1 } pa_kv_dtype;
 
+/* Implementations of the split-K producer (pa_select_producer). */
+typedef enum {
+  PA_PRODUCER_AUTO = 0, /* the tensor-core producer */
+  PA_PRODUCER_FMA = 1,  /* CUDA-core FMA producer: G in {1, 2, 4, 8} */
+  PA_PRODUCER_MMA = 2   /* tensor-core (mma.sync m16n8k16) producer: G in {1, 2, 4, 8, 16} */
+} pa_producer;
+
 /* Bits of the device-side error word (pa_read_error_flags). */
 #define PA_DEVERR_PAGE_OUT_OF_RANGE 0x1u     /* page_table entry outside [0, num_pages) */
 #define PA_DEVERR_POOL_ROW_OUT_OF_RANGE 0x2u /* req_pool_indices entry outside req_to_token */
@@ -154,7 +161,11 @@ pa_status pa_build_metadata_full(
  *   scratch_m, scratch_l [bs, num_q_heads, num_splits] fp32
  *   scratch_acc  [bs, num_q_heads, num_splits, head_dim] fp32
  * Supported: head_dim 128; page_size 16, 32, 64, 128; num_q_heads/num_kv_heads in
- * {1, 2, 4, 8}; otherwise PA_ERR_UNSUPPORTED.
+ * {1, 2, 4, 8, 16} (16 only with the tensor-core producer); otherwise
+ * PA_ERR_UNSUPPORTED.  Which producer implementation runs is chosen with
+ * pa_select_producer; both compute the same partials (to rounding).
+ * With use_pdl, q is read before the kernel waits on the previous grid (the prologue
+ * overlaps the metadata stage): the kernel launched just before must not write q.
  */
 pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
                            const float* k_scale, const float* v_scale, int32_t kv_dtype,
@@ -250,6 +261,13 @@ size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim,
  */
 int32_t pa_choose_splits(int32_t bs, int32_t num_kv_heads, int32_t max_seq_pages,
                          int32_t page_size, int32_t sm_count);
+
+/*
+ * Choose the split-K producer implementation for later calls in this process
+ * (PA_PRODUCER_AUTO, _FMA or _MMA); returns the previous choice.  An unknown value
+ * changes nothing and returns the current choice.  Meant for A/B measurement.
+ */
+int32_t pa_select_producer(int32_t producer);
 
 /* Static description of a status code. */
 const char* pa_status_string(pa_status status);

@@ -21,6 +21,7 @@ PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_SCRATCH_LIMIT = 0
 PA_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 PA_KV_BF16, PA_KV_INT8 = 0, 1
 PA_Q_MODE_NONE, PA_Q_MODE_CUMSUM, PA_Q_MODE_STRIDED = 0, 1, 2
+PA_PRODUCER_AUTO, PA_PRODUCER_FMA, PA_PRODUCER_MMA = 0, 1, 2
 DEVERR_PAGE_OUT_OF_RANGE = 0x1
 DEVERR_POOL_ROW_OUT_OF_RANGE = 0x2
 DEVERR_SLOT_OUT_OF_RANGE = 0x4
@@ -78,6 +79,8 @@ def _declare(lib):
     lib.pa_workspace_bytes.restype = sz
     lib.pa_choose_splits.argtypes = [i32, i32, i32, i32, i32]
     lib.pa_choose_splits.restype = i32
+    lib.pa_select_producer.argtypes = [i32]
+    lib.pa_select_producer.restype = i32
     lib.pa_status_string.argtypes = [i32]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_read_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
@@ -287,6 +290,26 @@ def pa_workspace_bytes(bs: int, num_q_heads: int, head_dim: int, num_splits: int
 def pa_choose_splits(bs: int, num_kv_heads: int, max_seq_pages: int, page_size: int,
                      sm_count: int = 0) -> int:
     return int(load().pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, sm_count))
+
+
+def pa_select_producer(producer: int) -> int:
+    """Choose the split-K producer implementation (PA_PRODUCER_AUTO / _FMA / _MMA) for
+    later calls; returns the previous choice."""
+    return int(load().pa_select_producer(int(producer)))
+
+
+class producer:
+    """Context manager: run a block with one producer implementation selected."""
+
+    def __init__(self, which: int):
+        self.which = which
+
+    def __enter__(self):
+        self.prev = pa_select_producer(self.which)
+        return self
+
+    def __exit__(self, *exc):
+        pa_select_producer(self.prev)
 
 
 def pa_status_string(status: int) -> str:

@@ -17,6 +17,7 @@ __device__ unsigned int g_pa_error_flags;
 
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned int*> g_err_ptr[kMaxDevices];
+std::atomic<int32_t> g_producer{PA_PRODUCER_AUTO};
 std::atomic<int> g_sm_count[kMaxDevices];
 
 cudaError_t error_word(unsigned int** out) {
@@ -104,7 +105,8 @@ pa_status check_attention(const void* q, const void* k_cache, const void* v_cach
   if (head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
     return PA_ERR_UNSUPPORTED;
-  if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+  if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
+    return PA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_seq_pages) * page_size > INT32_MAX) return PA_ERR_INVALID;
   return PA_OK;
 }
@@ -211,6 +213,9 @@ pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cac
   if (st != PA_OK || bs == 0) return st;
   if (!scratch_m || !scratch_l || !scratch_acc || !aligned16(scratch_acc))
     return PA_ERR_INVALID;
+  const int group = num_q_heads / num_kv_heads;
+  const bool use_fma = g_producer.load() == PA_PRODUCER_FMA;
+  if (use_fma && group > 8) return PA_ERR_UNSUPPORTED;
   pa::SplitKParams p = {};
   p.q = q;
   p.k_cache = k_cache;
@@ -232,12 +237,14 @@ pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cac
   p.acc_out = scratch_acc;
   cudaError_t e = error_word(&p.err);
   if (e != cudaSuccess) return PA_ERR_CUDA;
-  const int group = num_q_heads / num_kv_heads;
-  e = kv_dtype == PA_KV_INT8
-          ? pa::launch_splitk_int8(p, bs, group, page_size, static_cast<cudaStream_t>(stream),
-                                   use_pdl != 0)
-          : pa::launch_splitk_bf16(p, bs, group, page_size, static_cast<cudaStream_t>(stream),
-                                   use_pdl != 0);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kv_dtype == PA_KV_INT8) {
+    e = use_fma ? pa::launch_splitk_int8(p, bs, group, page_size, s, use_pdl != 0)
+                : pa::launch_splitk_mma_int8(p, bs, group, page_size, s, use_pdl != 0);
+  } else {
+    e = use_fma ? pa::launch_splitk_bf16(p, bs, group, page_size, s, use_pdl != 0)
+                : pa::launch_splitk_mma_bf16(p, bs, group, page_size, s, use_pdl != 0);
+  }
   if (e == cudaSuccess) e = cudaGetLastError();
   return from_cuda(e);
 }
@@ -341,6 +348,12 @@ pa_status pa_decode_step(
                         acc, stream, use_pdl);
   if (st != PA_OK) return st;
   return pa_reduce(m, l, acc, bs, num_q_heads, head_dim, splits, out, lse, stream, use_pdl);
+}
+
+int32_t pa_select_producer(int32_t producer) {
+  if (producer != PA_PRODUCER_AUTO && producer != PA_PRODUCER_FMA && producer != PA_PRODUCER_MMA)
+    return g_producer.load();
+  return g_producer.exchange(producer);
 }
 
 const char* pa_status_string(pa_status status) {

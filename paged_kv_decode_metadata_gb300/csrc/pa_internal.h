@@ -75,6 +75,11 @@ cudaError_t launch_splitk_bf16(const SplitKParams& p, int bs, int group, int pag
 cudaError_t launch_splitk_int8(const SplitKParams& p, int bs, int group, int page_size,
                                cudaStream_t stream, bool use_pdl);
 
+cudaError_t launch_splitk_mma_bf16(const SplitKParams& p, int bs, int group, int page_size,
+                                   cudaStream_t stream, bool use_pdl);
+cudaError_t launch_splitk_mma_int8(const SplitKParams& p, int bs, int group, int page_size,
+                                   cudaStream_t stream, bool use_pdl);
+
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool use_pdl);
 
 }  // namespace pa

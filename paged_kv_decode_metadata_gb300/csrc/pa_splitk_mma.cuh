@@ -1,0 +1,685 @@
+// Split-K paged-attention producer on the tensor cores (warp-level mma.sync).
+//
+// Same contract as the CUDA-core producer in pa_splitk.cuh (lmdeploy PR #4861,
+// "perf(cuda): use PDL for paged attention and V4 prefill", Changes: Split-K paged
+// attention): per split it writes the running max, the sum of exponentials and the
+// unnormalised accumulator, and signals its dependents before those final stores.
+//
+// Why tensor cores here: the G = Hq/Hkv query heads of a kv head turn QK^T and PV into
+// small dense contractions (G x 128 by 128 x tokens, and G x tokens by tokens x 128).
+// On CUDA cores every KV element costs G FMAs plus a widening conversion; at full HBM
+// rate that saturates the issue slots (G = 8 int8) or leaves the kernel latency bound
+// (G = 4 bf16).  One m16n8k16 MMA does 2048 multiply-adds per warp instruction.
+//
+// GB300 mapping
+//   * CTA = 4 consumer warps + 1 producer warp.  The producer warp's lane 0 streams
+//     64-token chunks with 4-D TMA tiled copies (cp.async.bulk.tensor) of the
+//     [num_pages, Hkv, page_size, 128] pools into a STAGES-deep ring; full/empty
+//     mbarriers hand stages back and forth, so there is no CTA-wide barrier per chunk.
+//     128-byte swizzle makes every ldmatrix / 16-byte shared load conflict free.
+//   * Consumer warp w owns tokens [16w, 16w+16) of every chunk and keeps its own
+//     online-softmax state (max, sum, output) for its tokens; the four states are
+//     merged once at the end of the split (the same log-sum-exp combination the
+//     reducer applies across splits).
+//   * Fragment layout follows the standard flash-attention register reuse: S = Q K^T
+//     with M = 16 query-head rows (rows >= G are zero), N = 8 tokens, K = 16 channels;
+//     the fp32 S fragment becomes, after the softmax, the A fragment of O += P V with
+//     K = 16 tokens, N = 8 channels.  Q fragments stay in registers for the whole split.
+//   * bf16 KV: K fragments come from ldmatrix, V fragments from ldmatrix.trans.
+//   * int8 KV: 16-byte shared loads of the codes, widened exactly to fp16 in registers
+//     (a byte placed in the mantissa of 1024, minus 1152) and fed to fp16 MMAs (int8
+//     codes are exact in fp16; Q is rounded to fp16, exact for 2^-14 <= |q| <= 65504).
+//     The contraction order over channels is permuted so that each lane reads
+//     16 contiguous bytes; QK^T does not depend on that order.  The K scale multiplies
+//     the fp32 score, the V scale folds into the softmax weight.
+//   * Scores are scaled in fp32 (sm_scale * log2 e), never by rounding Q.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include <atomic>
+#include <utility>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace mma {
+
+constexpr int kChunk = 64;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxSplitPages = 256;
+
+template <bool kQuant, int STAGES>
+struct Layout {
+  static constexpr int KV_BYTES = kQuant ? kChunk * 128 : kChunk * 256;  // per tensor per chunk
+  static constexpr int SCALE_BYTES = kQuant ? kChunk * 4 : 0;
+  static constexpr int STAGE_RAW = 2 * KV_BYTES + 2 * SCALE_BYTES;
+  static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;   // 1024-aligned tiles
+  static constexpr int OFF_PAGES = STAGES * STAGE_BYTES;
+  static constexpr int OFF_FULL = OFF_PAGES + kMaxSplitPages * 4;
+  static constexpr int OFF_EMPTY = OFF_FULL + STAGES * 8;
+  static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;                    // [4 warps][16 rows][2]
+  static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 2 * 4;    // abort flag, issued
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;                         // + alignment slack
+  static constexpr int RED_BYTES = kConsumerWarps * 16 * 128 * 4;           // output merge buffer
+  static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "merge buffer reuses the ring");
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <bool kF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (kF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void consumer_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// Two bf16/fp16 values packed low-first.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two biased int8 codes (already XORed with 0x80) -> fp16x2 holding the signed codes:
+// each byte becomes the low mantissa byte of 1024, then 1152 is subtracted (exact).
+__device__ __forceinline__ uint32_t biased_bytes_to_f16x2(uint32_t x, uint32_t selector) {
+  const uint32_t h = __byte_perm(x, 0x64646464u, selector);
+  __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), __float2half2_rn(1152.f));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-row tile written by
+// TMA with 128-byte swizzle (the tile starts on a 1024-byte boundary).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+template <bool kQuant, int P, int STAGES, int MINB, bool kRows16>
+__global__ void __launch_bounds__(kThreads, MINB)
+    splitk_mma_kernel(const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_v, const SplitKParams prm) {
+  using L = Layout<kQuant, STAGES>;
+  constexpr bool kF16 = kQuant;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t smem_base = smem_addr(smem);
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int G = prm.num_q_heads / prm.num_kv_heads;
+  const int S = prm.num_splits;
+  const bool is_consumer = warp < kConsumerWarps;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_FULL);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L::OFF_EMPTY);
+  int32_t* pages_s = reinterpret_cast<int32_t*>(smem + L::OFF_PAGES);
+  float* ml_s = reinterpret_cast<float*>(smem + L::OFF_ML);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC);
+  int* issued_s = reinterpret_cast<int*>(smem + L::OFF_MISC + 4);
+
+  // ---- prologue independent of the metadata stage: Q fragments in registers --------
+  uint32_t qa[8][4];
+  if (is_consumer) {
+    const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(prm.q) +
+                                 (static_cast<int64_t>(b) * prm.num_q_heads + kvh * G) * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int row = gid + 8 * half;
+        uint32_t lo = 0, hi = 0;
+        if (row < G && (half == 0 || kRows16)) {
+          const __nv_bfloat16* qr = qbase + row * 128;
+          if constexpr (kF16) {
+            // contraction order: k-step j, lane tig -> channels 32*tig + 4*j + {0..3}
+            const int d = 32 * tig + 4 * j;
+            lo = pack_f16(__bfloat162float(qr[d]), __bfloat162float(qr[d + 1]));
+            hi = pack_f16(__bfloat162float(qr[d + 2]), __bfloat162float(qr[d + 3]));
+          } else {
+            const int d = 16 * j + 2 * tig;
+            lo = *reinterpret_cast<const uint32_t*>(qr + d);
+            hi = *reinterpret_cast<const uint32_t*>(qr + d + 8);
+          }
+        }
+        qa[j][half] = lo;       // a0 (row gid) / a1 (row gid + 8)
+        qa[j][2 + half] = hi;   // a2 (row gid) / a3 (row gid + 8)
+      }
+    }
+  }
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    *abort_flag = 0;
+    *issued_s = 0;
+    fence_barrier_init();
+  }
+
+  // ---- everything below reads what the metadata stage wrote -------------------------
+  grid_dependency_wait();
+
+  int n = prm.cache_seqlens[b];
+  const int cap = prm.max_seq_pages * P;
+  if (n < 0 || n > cap) {
+    if (tid == 0 && split == 0 && kvh == 0) record_error(prm.err, kErrSeqLenOutOfRange);
+    n = n < 0 ? 0 : cap;
+  }
+  const int n_pages = (n + P - 1) / P;
+  const int p_begin = split * prm.pages_per_split;
+  const int p_end = min(p_begin + prm.pages_per_split, n_pages);
+  const int tok_begin = p_begin * P;
+  const int n_tok = min(p_end * P, n) - tok_begin;
+  const int64_t slot0 =
+      (static_cast<int64_t>(b) * prm.num_q_heads + kvh * G) * S + split;
+
+  if (n_tok <= 0) {
+    trigger_dependents();
+    if (tid < G) {
+      prm.m_out[slot0 + static_cast<int64_t>(tid) * S] = -CUDART_INF_F;
+      prm.l_out[slot0 + static_cast<int64_t>(tid) * S] = 0.f;
+    }
+    return;
+  }
+
+  const int n_split_pages = p_end - p_begin;
+  const int32_t* pt_row =
+      prm.page_table + static_cast<int64_t>(b) * prm.page_table_stride + p_begin;
+  for (int i = tid; i < min(n_split_pages, kMaxSplitPages); i += kThreads) {
+    int32_t pg = pt_row[i];
+    if (pg < 0 || pg >= prm.num_pages) {
+      record_error(prm.err, kErrPageOutOfRange);
+      pg = 0;
+    }
+    pages_s[i] = pg;
+  }
+  __syncthreads();  // barriers initialised, page indices cached
+
+  const int n_chunks = (n_tok + kChunk - 1) / kChunk;
+
+  // ======================= producer warp: TMA issue loop ============================
+  if (!is_consumer) {
+    if (lane == 0) {
+      const uint64_t policy = l2_evict_first_policy();
+      int c = 0;
+      for (; c < n_chunks; ++c) {
+        const int stage = c % STAGES;
+        if (c >= STAGES) {
+          const uint32_t parity = static_cast<uint32_t>(c / STAGES - 1) & 1u;
+          if (!mbar_wait_bounded(&empty[stage], parity) || *abort_flag) {
+            record_error(prm.err, kErrWaitTimeout);
+            *abort_flag = 1;
+            break;
+          }
+        }
+        const uint32_t kdst = smem_base + stage * L::STAGE_BYTES;
+        const uint32_t vdst = kdst + L::KV_BYTES;
+        const int ctok = c * kChunk;
+        auto page_at = [&](int i) -> int {
+          if (i < kMaxSplitPages) return pages_s[i];
+          int32_t pg = pt_row[i];
+          if (pg < 0 || pg >= prm.num_pages) {
+            record_error(prm.err, kErrPageOutOfRange);
+            pg = 0;
+          }
+          return pg;
+        };
+        if constexpr (P >= kChunk) {
+          const int pg = page_at(ctok / P);
+          const int row = ctok % P;
+          mbar_arrive_expect_tx(&full[stage], 2 * L::KV_BYTES + 2 * L::SCALE_BYTES);
+          if constexpr (kQuant) {
+            tma_load_4d(kdst, &map_k, 0, row, kvh, pg, &full[stage], policy);
+            tma_load_4d(vdst, &map_v, 0, row, kvh, pg, &full[stage], policy);
+            const int64_t srow = (static_cast<int64_t>(pg) * prm.num_kv_heads + kvh) * P + row;
+            unsigned char* st = smem + stage * L::STAGE_BYTES;
+            bulk_copy_g2s(st + 2 * L::KV_BYTES, prm.k_scale + srow, L::SCALE_BYTES, &full[stage],
+                          policy);
+            bulk_copy_g2s(st + 2 * L::KV_BYTES + L::SCALE_BYTES, prm.v_scale + srow,
+                          L::SCALE_BYTES, &full[stage], policy);
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              tma_load_4d(kdst + h * 8192, &map_k, 64 * h, row, kvh, pg, &full[stage], policy);
+              tma_load_4d(vdst + h * 8192, &map_v, 64 * h, row, kvh, pg, &full[stage], policy);
+            }
+          }
+        } else {
+          constexpr int kPages = kChunk / P;
+          const int first = ctok / P;
+          const int np = min(kPages, n_split_pages - first);
+          constexpr int kPageRows = P * 128;  // bytes of one page's rows in a 128-B-row tile
+          mbar_arrive_expect_tx(&full[stage],
+                                np * (kQuant ? 2 * (P * 128 + P * 4) : 2 * P * 256));
+          for (int k = 0; k < np; ++k) {
+            const int pg = page_at(first + k);
+            if constexpr (kQuant) {
+              tma_load_4d(kdst + k * kPageRows, &map_k, 0, 0, kvh, pg, &full[stage], policy);
+              tma_load_4d(vdst + k * kPageRows, &map_v, 0, 0, kvh, pg, &full[stage], policy);
+              const int64_t srow = (static_cast<int64_t>(pg) * prm.num_kv_heads + kvh) * P;
+              unsigned char* st = smem + stage * L::STAGE_BYTES;
+              bulk_copy_g2s(st + 2 * L::KV_BYTES + k * P * 4, prm.k_scale + srow, P * 4,
+                            &full[stage], policy);
+              bulk_copy_g2s(st + 2 * L::KV_BYTES + L::SCALE_BYTES + k * P * 4,
+                            prm.v_scale + srow, P * 4, &full[stage], policy);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                tma_load_4d(kdst + h * 8192 + k * kPageRows, &map_k, 64 * h, 0, kvh, pg,
+                            &full[stage], policy);
+                tma_load_4d(vdst + h * 8192 + k * kPageRows, &map_v, 64 * h, 0, kvh, pg,
+                            &full[stage], policy);
+              }
+            }
+          }
+        }
+      }
+      *issued_s = c;
+    }
+    trigger_dependents();
+    return;
+  }
+
+  // ======================= consumer warps =============================================
+  float o[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};  // rows gid, gid + 8
+  float l_part[2] = {0.f, 0.f};
+  const float q_scale = prm.q_scale;
+  const int t0 = warp * 16;  // this warp's tokens inside every chunk
+  bool failed = false;
+
+  for (int c = 0; c < n_chunks; ++c) {
+    const int stage = c % STAGES;
+    if (!mbar_wait_bounded(&full[stage], static_cast<uint32_t>(c / STAGES) & 1u) || *abort_flag) {
+      if (lane == 0) {
+        record_error(prm.err, kErrWaitTimeout);
+        *abort_flag = 1;
+      }
+      failed = true;
+      break;
+    }
+    const int valid = min(kChunk, n_tok - c * kChunk);
+    unsigned char* st = smem + stage * L::STAGE_BYTES;
+    const uint32_t kst = smem_base + stage * L::STAGE_BYTES;
+    const uint32_t vst = kst + L::KV_BYTES;
+
+    if (t0 < valid) {
+      // Rows of this warp's slice past the context: their V bytes are not ours to trust
+      // (stale ring contents or cache slots past the request), so zero them before PV.
+      if (valid < t0 + 16) {
+        for (int r = max(valid, t0) + (lane >> 3); r < t0 + 16; r += 4) {
+          uint4* row = reinterpret_cast<uint4*>(st + L::KV_BYTES + r * 128);
+          row[lane & 7] = make_uint4(0u, 0u, 0u, 0u);
+          if constexpr (!kQuant) {
+            uint4* row2 = reinterpret_cast<uint4*>(st + L::KV_BYTES + 8192 + r * 128);
+            row2[lane & 7] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        __syncwarp();
+      }
+
+      // ---- S = Q K^T for tokens t0..t0+15 (two n-tiles of 8) ----------------------
+      float sfr[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) sfr[nt][0] = sfr[nt][1] = sfr[nt][2] = sfr[nt][3] = 0.f;
+      if constexpr (!kQuant) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // 32 channels per step: two k-steps
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const int row = t0 + 8 * nt + (lane & 7);
+            const int chunk = 4 * kk + (lane >> 3);  // 16-byte chunk of the 256-byte row
+            const uint32_t addr = kst + (chunk >> 3) * 8192 + swz(row, chunk & 7);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(addr, b0, b1, b2, b3);
+            mma16816<false>(sfr[nt], qa[2 * kk], b0, b1);
+            mma16816<false>(sfr[nt], qa[2 * kk + 1], b2, b3);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int row = t0 + 8 * nt + gid;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(st + swz(row, 2 * tig));
+          const uint4 w1 = *reinterpret_cast<const uint4*>(st + swz(row, 2 * tig + 1));
+          const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t x = words[j] ^ 0x80808080u;
+            mma16816<true>(sfr[nt], qa[j], biased_bytes_to_f16x2(x, 0x4140),
+                           biased_bytes_to_f16x2(x, 0x4342));
+          }
+        }
+      }
+
+      // ---- online softmax (base 2) over this warp's 16 tokens ---------------------
+      const float* kscale = reinterpret_cast<const float*>(st + 2 * L::KV_BYTES);
+      const float* vscale = kscale + kChunk;
+      float p[2][4];
+      float alpha[2];
+#pragma unroll
+      for (int hr = 0; hr < (kRows16 ? 2 : 1); ++hr) {
+        float x[4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tok = t0 + 8 * nt + 2 * tig + e;
+            float v = sfr[nt][2 * hr + e] * q_scale;
+            if constexpr (kQuant) v *= kscale[tok];
+            x[2 * nt + e] = tok < valid ? v : -CUDART_INF_F;
+          }
+        }
+        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run[hr], mx);
+        if (m_new == -CUDART_INF_F) {
+          alpha[hr] = 1.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) p[hr][i] = 0.f;
+        } else {
+          alpha[hr] = exp2f(m_run[hr] - m_new);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) p[hr][i] = exp2f(x[i] - m_new);
+        }
+        l_part[hr] = l_part[hr] * alpha[hr] + (p[hr][0] + p[hr][1]) + (p[hr][2] + p[hr][3]);
+        m_run[hr] = m_new;
+      }
+      if (!kRows16) {
+        alpha[1] = 1.f;
+        p[1][0] = p[1][1] = p[1][2] = p[1][3] = 0.f;
+      }
+      if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          o[j][0] *= alpha[0];
+          o[j][1] *= alpha[0];
+          o[j][2] *= alpha[1];
+          o[j][3] *= alpha[1];
+        }
+      }
+
+      // ---- O += P V ----------------------------------------------------------------
+      uint32_t pa[4];
+      if constexpr (kQuant) {
+        float vs[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = t0 + 8 * (i >> 1) + 2 * tig + (i & 1);
+          vs[i] = tok < valid ? vscale[tok] : 0.f;
+        }
+        pa[0] = pack_f16(p[0][0] * vs[0], p[0][1] * vs[1]);
+        pa[1] = pack_f16(p[1][0] * vs[0], p[1][1] * vs[1]);
+        pa[2] = pack_f16(p[0][2] * vs[2], p[0][3] * vs[3]);
+        pa[3] = pack_f16(p[1][2] * vs[2], p[1][3] * vs[3]);
+        // V rows t0 + 2tig + {0, 1, 8, 9}, channels 16*gid .. 16*gid + 15
+        const int r0 = t0 + 2 * tig;
+        const uint4 va = *reinterpret_cast<const uint4*>(st + L::KV_BYTES + swz(r0, gid));
+        const uint4 vb = *reinterpret_cast<const uint4*>(st + L::KV_BYTES + swz(r0 + 1, gid));
+        const uint4 vc = *reinterpret_cast<const uint4*>(st + L::KV_BYTES + swz(r0 + 8, gid));
+        const uint4 vd = *reinterpret_cast<const uint4*>(st + L::KV_BYTES + swz(r0 + 9, gid));
+        const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+        const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t xa = wa[w] ^ 0x80808080u, xb = wb[w] ^ 0x80808080u;
+          const uint32_t xc = wc[w] ^ 0x80808080u, xd = wd[w] ^ 0x80808080u;
+          const uint32_t ab_lo = __byte_perm(xa, xb, 0x5140), ab_hi = __byte_perm(xa, xb, 0x7362);
+          const uint32_t cd_lo = __byte_perm(xc, xd, 0x5140), cd_hi = __byte_perm(xc, xd, 0x7362);
+          // n-tile j = 4w + k covers channel 16*gid + j
+          mma16816<true>(o[4 * w + 0], pa, biased_bytes_to_f16x2(ab_lo, 0x4140),
+                         biased_bytes_to_f16x2(cd_lo, 0x4140));
+          mma16816<true>(o[4 * w + 1], pa, biased_bytes_to_f16x2(ab_lo, 0x4342),
+                         biased_bytes_to_f16x2(cd_lo, 0x4342));
+          mma16816<true>(o[4 * w + 2], pa, biased_bytes_to_f16x2(ab_hi, 0x4140),
+                         biased_bytes_to_f16x2(cd_hi, 0x4140));
+          mma16816<true>(o[4 * w + 3], pa, biased_bytes_to_f16x2(ab_hi, 0x4342),
+                         biased_bytes_to_f16x2(cd_hi, 0x4342));
+        }
+      } else {
+        pa[0] = pack_bf16(p[0][0], p[0][1]);
+        pa[1] = pack_bf16(p[1][0], p[1][1]);
+        pa[2] = pack_bf16(p[0][2], p[0][3]);
+        pa[3] = pack_bf16(p[1][2], p[1][3]);
+#pragma unroll
+        for (int dp = 0; dp < 8; ++dp) {  // 16 channels per step: two n-tiles
+          const int mi = lane >> 3;
+          const int row = t0 + (lane & 7) + 8 * (mi & 1);
+          const int chunk = 2 * dp + (mi >> 1);
+          const uint32_t addr = vst + (chunk >> 3) * 8192 + swz(row, chunk & 7);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_trans(addr, b0, b1, b2, b3);
+          mma16816<false>(o[2 * dp], pa, b0, b1);
+          mma16816<false>(o[2 * dp + 1], pa, b2, b3);
+        }
+      }
+    }
+    // this warp is done with the stage; zeroing stores (generic proxy) must be ordered
+    // before the TMA (async proxy) refills the buffer
+    if (t0 < valid && valid < t0 + 16) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+  }
+
+  trigger_dependents();
+
+  // ---- merge the four warps' softmax states, write the split's partials -------------
+  float l_row[2];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    float v = l_part[hr];
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    l_row[hr] = v;
+  }
+  if (tig == 0) {
+    ml_s[(warp * 16 + gid) * 2 + 0] = m_run[0];
+    ml_s[(warp * 16 + gid) * 2 + 1] = l_row[0];
+    ml_s[(warp * 16 + gid + 8) * 2 + 0] = m_run[1];
+    ml_s[(warp * 16 + gid + 8) * 2 + 1] = l_row[1];
+  }
+  consumer_barrier();
+  if (failed || *abort_flag) {
+    // Drain what the producer issued so no TMA write lands after the CTA exits.
+    if (tid == 0) {
+      for (int c = 0; c < n_chunks; ++c) {
+        if (!mbar_wait_bounded(&full[c % STAGES], static_cast<uint32_t>(c / STAGES) & 1u)) break;
+      }
+    }
+    return;
+  }
+  float* red = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][128]
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int row = gid + 8 * hr;
+    float mrow = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + row) * 2]);
+    const float scale = m_run[hr] == -CUDART_INF_F ? 0.f : exp2f(m_run[hr] - mrow);
+    float* dst = red + (warp * 16 + row) * 128;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if constexpr (kQuant) {
+        dst[32 * tig + j] = o[j][2 * hr] * scale;         // channel 16*(2tig) + j
+        dst[32 * tig + 16 + j] = o[j][2 * hr + 1] * scale; // channel 16*(2tig+1) + j
+      } else {
+        *reinterpret_cast<float2*>(dst + 8 * j + 2 * tig) =
+            make_float2(o[j][2 * hr] * scale, o[j][2 * hr + 1] * scale);
+      }
+    }
+  }
+  consumer_barrier();
+  for (int idx = tid; idx < G * 32; idx += kConsumerWarps * 32) {
+    const int row = idx >> 5, d = (idx & 31) * 4;
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float4 v = *reinterpret_cast<const float4*>(red + (w * 16 + row) * 128 + d);
+      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+    }
+    *reinterpret_cast<float4*>(prm.acc_out + (slot0 + static_cast<int64_t>(row) * S) * 128 + d) =
+        sum;
+  }
+  if (tid < G) {
+    float mrow = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + tid) * 2]);
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = ml_s[(w * 16 + tid) * 2];
+      if (mw != -CUDART_INF_F) lsum += ml_s[(w * 16 + tid) * 2 + 1] * exp2f(mw - mrow);
+    }
+    prm.m_out[slot0 + static_cast<int64_t>(tid) * S] = mrow * 0.69314718055994530942f;
+    prm.l_out[slot0 + static_cast<int64_t>(tid) * S] = lsum;
+  }
+}
+
+// ---- host side ------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_tiled_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load();
+  if (f == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      return nullptr;
+    }
+    f = reinterpret_cast<EncodeTiledFn>(p);
+    fn.store(f);
+  }
+  return f;
+}
+
+// Tensor map over a [num_pages, Hkv, P, 128] pool: box of 64 (bf16) or 128 (int8)
+// channels by min(P, 64) rows of one (page, kv head), 128-byte swizzle.
+inline cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, bool quant, int64_t num_pages,
+                                   int num_kv_heads, int page_size) {
+  EncodeTiledFn encode = encode_tiled_fn();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t esz = quant ? 1 : 2;
+  const cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(page_size),
+                              static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[3] = {128 * esz, 128 * esz * page_size,
+                                 128 * esz * page_size * num_kv_heads};
+  const cuuint32_t box[4] = {quant ? 128u : 64u,
+                             static_cast<cuuint32_t>(page_size < kChunk ? page_size : kChunk), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = encode(map, quant ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                            4, const_cast<void*>(pool), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool kQuant, int P, int STAGES, int MINB, bool kRows16>
+cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
+                           dim3 grid, cudaStream_t stream, bool use_pdl) {
+  using L = Layout<kQuant, STAGES>;
+  void (*kernel)(const CUtensorMap, const CUtensorMap, const SplitKParams) =
+      splitk_mma_kernel<kQuant, P, STAGES, MINB, kRows16>;
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if ((configured.load() & bit) == 0) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
+  return launch_kernel(kernel, grid, dim3(kThreads), static_cast<size_t>(L::SMEM), stream,
+                       use_pdl, mk, mv, p);
+}
+
+template <bool kQuant, int STAGES, int MINB>
+cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_size,
+                            cudaStream_t stream, bool use_pdl) {
+  CUtensorMap mk, mv;
+  cudaError_t e = encode_pool_map(&mk, p.k_cache, kQuant, p.num_pages, p.num_kv_heads, page_size);
+  if (e != cudaSuccess) return e;
+  e = encode_pool_map(&mv, p.v_cache, kQuant, p.num_pages, p.num_kv_heads, page_size);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(p.num_splits), static_cast<unsigned>(p.num_kv_heads),
+                  static_cast<unsigned>(bs));
+  const bool rows16 = group > 8;
+#define PA_MMA_CASE(PP)                                                                     \
+  if (page_size == PP) {                                                                    \
+    return rows16 ? launch_mma_one<kQuant, PP, STAGES, MINB, true>(p, mk, mv, grid, stream, \
+                                                                   use_pdl)                 \
+                  : launch_mma_one<kQuant, PP, STAGES, MINB, false>(p, mk, mv, grid, stream, \
+                                                                    use_pdl);               \
+  }
+  PA_MMA_CASE(16)
+  PA_MMA_CASE(32)
+  PA_MMA_CASE(64)
+  PA_MMA_CASE(128)
+#undef PA_MMA_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mma
+}  // namespace pa

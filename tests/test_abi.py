@@ -60,7 +60,16 @@ def test_splitk_host_validation(lib):
     assert _splitk(lib, kv=1) == B.PA_ERR_INVALID             # int8 without scales
     assert _splitk(lib, d=64) == B.PA_ERR_UNSUPPORTED
     assert _splitk(lib, P=48) == B.PA_ERR_UNSUPPORTED
-    assert _splitk(lib, hq=128) == B.PA_ERR_UNSUPPORTED       # group 16
+    assert _splitk(lib, hq=256) == B.PA_ERR_UNSUPPORTED       # group 32
+    with B.producer(B.PA_PRODUCER_FMA):
+        assert _splitk(lib, hq=128) == B.PA_ERR_UNSUPPORTED   # group 16: tensor-core only
+
+
+def test_producer_selection(lib):
+    prev = B.pa_select_producer(B.PA_PRODUCER_FMA)
+    assert B.pa_select_producer(B.PA_PRODUCER_MMA) == B.PA_PRODUCER_FMA
+    assert B.pa_select_producer(7) == B.PA_PRODUCER_MMA          # unknown: no change
+    assert B.pa_select_producer(prev) == B.PA_PRODUCER_MMA
 
 
 def test_reduce_and_metadata_host_validation(lib):

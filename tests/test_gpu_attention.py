@@ -50,12 +50,17 @@ def _check_flags():
     assert B.pa_read_error_flags(reset=True) == 0
 
 
+PRODUCERS = {"mma": B.PA_PRODUCER_MMA, "fma": B.PA_PRODUCER_FMA}
+
+
 # ---- whole step on the five workloads --------------------------------------------------
 
+@pytest.mark.parametrize("impl", sorted(PRODUCERS))
 @pytest.mark.parametrize("name", synthetic.WORKLOAD_ORDER)
-def test_decode_step_matches_oracle(name):
+def test_decode_step_matches_oracle(name, impl):
     wl, ds = named(name)
-    ds.step(use_pdl=True)
+    with B.producer(PRODUCERS[impl]):
+        ds.step(use_pdl=True)
     torch.cuda.synchronize()
     _check_flags()
     meta = oracle_metadata(wl)
@@ -68,11 +73,13 @@ def test_decode_step_matches_oracle(name):
     assert_attention_close(ds.out[rows], ds.lse[rows], out_ref, lse_ref, name)
 
 
+@pytest.mark.parametrize("impl", sorted(PRODUCERS))
 @pytest.mark.parametrize("name", ["bs1_ctx1k", "bs8_ctx1k", "bs1_ctx8k"])
-def test_splitk_scratch_matches_oracle_partials(name):
+def test_splitk_scratch_matches_oracle_partials(name, impl):
     wl, ds = named(name)
     ds.metadata()
-    ds.splitk()
+    with B.producer(PRODUCERS[impl]):
+        ds.splitk()
     torch.cuda.synchronize()
     _check_flags()
     meta = oracle_metadata(wl)
@@ -114,15 +121,20 @@ def test_reduce_alone_matches_oracle_combine():
 # ---- small random shapes: every group size, page size and KV type ---------------------
 
 SMALL = [(seed, kv, grp, P) for seed, (kv, grp, P) in enumerate(
-    [(kv, grp, P) for kv in ("bf16", "int8") for grp in (1, 2, 4, 8) for P in (16, 32, 64, 128)])]
+    [(kv, grp, P) for kv in ("bf16", "int8") for grp in (1, 2, 4, 8, 16)
+     for P in (16, 32, 64, 128)])]
 
 
+@pytest.mark.parametrize("impl", sorted(PRODUCERS))
 @pytest.mark.parametrize("seed,kv,grp,P", SMALL)
-def test_small_shapes_match_oracle(seed, kv, grp, P):
+def test_small_shapes_match_oracle(seed, kv, grp, P, impl):
+    if impl == "fma" and grp > 8:
+        pytest.skip("the CUDA-core producer covers G <= 8")
     spec = synthetic.small_spec(500 + seed, kv_dtype=kv, group=grp, page_size=P, ctx_max=330)
     wl = synthetic.make(spec)
     ds = DeviceStep(wl, page_table_stride=wl.max_seq_pages + 2)
-    ds.step()
+    with B.producer(PRODUCERS[impl]):
+        ds.step()
     torch.cuda.synchronize()
     _check_flags()
     meta = oracle_metadata(wl)
@@ -132,6 +144,7 @@ def test_small_shapes_match_oracle(seed, kv, grp, P):
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 5, 16, 40])
 def test_split_count_does_not_change_result(splits):
+    """Default (tensor-core) producer."""
     spec = synthetic.Spec("splits", bs=3, num_q_heads=16, num_kv_heads=4, num_pages=40,
                           ragged=(100, 700), num_splits=splits, seed=900)
     wl = synthetic.make(spec)
