@@ -43,11 +43,12 @@ def library_path() -> str:
 
 
 def load() -> ctypes.CDLL:
-    """Load libpa.so (built by ``build.build()``); raise if it is not there."""
+    """Load libpa.so (built by ``build.build()``, or the file named by the PA_LIBRARY
+    environment variable); raise if it is not there."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB_PATH
+            path = os.environ.get("PA_LIBRARY") or _build.LIB_PATH
             if not os.path.exists(path):
                 raise RuntimeError(
                     f"CUDA library {path} is missing; build it with "

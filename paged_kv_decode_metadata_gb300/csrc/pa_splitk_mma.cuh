@@ -115,6 +115,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Transpose an 8x8 matrix of 16-bit values held in the standard fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ void consumer_barrier() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
@@ -143,7 +150,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <bool kQuant, int P, int STAGES, int MINB, bool kRows16>
+template <bool kQuant, int P, int STAGES, int MINB, int kNT>
 __global__ void __launch_bounds__(kThreads, MINB)
     splitk_mma_kernel(const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const SplitKParams prm) {
@@ -166,35 +173,33 @@ __global__ void __launch_bounds__(kThreads, MINB)
   int32_t* pages_s = reinterpret_cast<int32_t*>(smem + L::OFF_PAGES);
   float* ml_s = reinterpret_cast<float*>(smem + L::OFF_ML);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC);
-  int* issued_s = reinterpret_cast<int*>(smem + L::OFF_MISC + 4);
 
-  // ---- prologue independent of the metadata stage: Q fragments in registers --------
-  uint32_t qa[8][4];
-  if (is_consumer) {
-    const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(prm.q) +
-                                 (static_cast<int64_t>(b) * prm.num_q_heads + kvh * G) * 128;
+  // ---- prologue independent of the metadata stage: Q^T fragments in registers ------
+  // B operand of S^T = K Q^T: b0 = Q[head][k 2tig, 2tig+1], b1 = Q[head][k 2tig+8, +9]
+  // of k-step j, head = 8 * nt + gid.
+  uint32_t qb[kNT][8][2];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+    const int head = 8 * nt + gid;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int row = gid + 8 * half;
-        uint32_t lo = 0, hi = 0;
-        if (row < G && (half == 0 || kRows16)) {
-          const __nv_bfloat16* qr = qbase + row * 128;
-          if constexpr (kF16) {
-            // contraction order: k-step j, lane tig -> channels 32*tig + 4*j + {0..3}
-            const int d = 32 * tig + 4 * j;
-            lo = pack_f16(__bfloat162float(qr[d]), __bfloat162float(qr[d + 1]));
-            hi = pack_f16(__bfloat162float(qr[d + 2]), __bfloat162float(qr[d + 3]));
-          } else {
-            const int d = 16 * j + 2 * tig;
-            lo = *reinterpret_cast<const uint32_t*>(qr + d);
-            hi = *reinterpret_cast<const uint32_t*>(qr + d + 8);
-          }
+      uint32_t lo = 0, hi = 0;
+      if (is_consumer && head < G) {
+        const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(prm.q) +
+                                  (static_cast<int64_t>(b) * prm.num_q_heads + kvh * G + head) * 128;
+        if constexpr (kF16) {
+          // contraction order: k-step j, lane tig -> channels 32*tig + 4*j + {0..3}
+          const int d = 32 * tig + 4 * j;
+          lo = pack_f16(__bfloat162float(qr[d]), __bfloat162float(qr[d + 1]));
+          hi = pack_f16(__bfloat162float(qr[d + 2]), __bfloat162float(qr[d + 3]));
+        } else {
+          const int d = 16 * j + 2 * tig;
+          lo = *reinterpret_cast<const uint32_t*>(qr + d);
+          hi = *reinterpret_cast<const uint32_t*>(qr + d + 8);
         }
-        qa[j][half] = lo;       // a0 (row gid) / a1 (row gid + 8)
-        qa[j][2 + half] = hi;   // a2 (row gid) / a3 (row gid + 8)
       }
+      qb[nt][j][0] = lo;
+      qb[nt][j][1] = hi;
     }
   }
   if (tid == 0) {
@@ -203,7 +208,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
       mbar_init(&empty[s], kConsumerWarps);
     }
     *abort_flag = 0;
-    *issued_s = 0;
     fence_barrier_init();
   }
 
@@ -252,8 +256,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   if (!is_consumer) {
     if (lane == 0) {
       const uint64_t policy = l2_evict_first_policy();
-      int c = 0;
-      for (; c < n_chunks; ++c) {
+      for (int c = 0; c < n_chunks; ++c) {
         const int stage = c % STAGES;
         if (c >= STAGES) {
           const uint32_t parity = static_cast<uint32_t>(c / STAGES - 1) & 1u;
@@ -325,18 +328,25 @@ __global__ void __launch_bounds__(kThreads, MINB)
           }
         }
       }
-      *issued_s = c;
     }
     trigger_dependents();
     return;
   }
 
   // ======================= consumer warps =============================================
-  float o[16][4];
+  // O^T[channel][head] fragments: M-tile i covers 16 channels, n-tile nt 8 heads.
+  float o[kNT][8][4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};  // rows gid, gid + 8
-  float l_part[2] = {0.f, 0.f};
+  for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
+  // softmax state of heads 8*nt + 2*tig + e (identical in the 8 lanes sharing tig)
+  float m_run[kNT][2], l_part[kNT][2];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+    m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
+    l_part[nt][0] = l_part[nt][1] = 0.f;
+  }
   const float q_scale = prm.q_scale;
   const int t0 = warp * 16;  // this warp's tokens inside every chunk
   bool failed = false;
@@ -355,11 +365,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
     unsigned char* st = smem + stage * L::STAGE_BYTES;
     const uint32_t kst = smem_base + stage * L::STAGE_BYTES;
     const uint32_t vst = kst + L::KV_BYTES;
+    const bool partial = valid < t0 + 16;
 
     if (t0 < valid) {
       // Rows of this warp's slice past the context: their V bytes are not ours to trust
       // (stale ring contents or cache slots past the request), so zero them before PV.
-      if (valid < t0 + 16) {
+      if (partial) {
         for (int r = max(valid, t0) + (lane >> 3); r < t0 + 16; r += 4) {
           uint4* row = reinterpret_cast<uint4*>(st + L::KV_BYTES + r * 128);
           row[lane & 7] = make_uint4(0u, 0u, 0u, 0u);
@@ -371,102 +382,114 @@ __global__ void __launch_bounds__(kThreads, MINB)
         __syncwarp();
       }
 
-      // ---- S = Q K^T for tokens t0..t0+15 (two n-tiles of 8) ----------------------
-      float sfr[2][4];
+      // ---- S^T = K Q^T for tokens t0..t0+15 (M = 16 tokens, N = 8 heads per n-tile) --
+      // two accumulators (even / odd k-steps) halve the dependent MMA chain
+      float acc[2][kNT][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) sfr[nt][0] = sfr[nt][1] = sfr[nt][2] = sfr[nt][3] = 0.f;
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) acc[a][nt][0] = acc[a][nt][1] = acc[a][nt][2] = acc[a][nt][3] = 0.f;
       if constexpr (!kQuant) {
+        const int mi = lane >> 3;
+        const int row = t0 + (lane & 7) + 8 * (mi & 1);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 32 channels per step: two k-steps
+        for (int j = 0; j < 8; ++j) {
+          const int chunk = 2 * j + (mi >> 1);  // 16-byte chunk of the 256-byte row
+          const uint32_t addr = kst + (chunk >> 3) * 8192 + swz(row, chunk & 7);
+          uint32_t a[4];
+          ldsm_x4(addr, a[0], a[1], a[2], a[3]);
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const int row = t0 + 8 * nt + (lane & 7);
-            const int chunk = 4 * kk + (lane >> 3);  // 16-byte chunk of the 256-byte row
-            const uint32_t addr = kst + (chunk >> 3) * 8192 + swz(row, chunk & 7);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(addr, b0, b1, b2, b3);
-            mma16816<false>(sfr[nt], qa[2 * kk], b0, b1);
-            mma16816<false>(sfr[nt], qa[2 * kk + 1], b2, b3);
-          }
+          for (int nt = 0; nt < kNT; ++nt) mma16816<false>(acc[j & 1][nt], a, qb[nt][j][0], qb[nt][j][1]);
         }
       } else {
+        const uint4 r0a = *reinterpret_cast<const uint4*>(st + swz(t0 + gid, 2 * tig));
+        const uint4 r0b = *reinterpret_cast<const uint4*>(st + swz(t0 + gid, 2 * tig + 1));
+        const uint4 r1a = *reinterpret_cast<const uint4*>(st + swz(t0 + gid + 8, 2 * tig));
+        const uint4 r1b = *reinterpret_cast<const uint4*>(st + swz(t0 + gid + 8, 2 * tig + 1));
+        const uint32_t w0[8] = {r0a.x, r0a.y, r0a.z, r0a.w, r0b.x, r0b.y, r0b.z, r0b.w};
+        const uint32_t w1[8] = {r1a.x, r1a.y, r1a.z, r1a.w, r1b.x, r1b.y, r1b.z, r1b.w};
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int row = t0 + 8 * nt + gid;
-          const uint4 w0 = *reinterpret_cast<const uint4*>(st + swz(row, 2 * tig));
-          const uint4 w1 = *reinterpret_cast<const uint4*>(st + swz(row, 2 * tig + 1));
-          const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t x0 = w0[j] ^ 0x80808080u, x1 = w1[j] ^ 0x80808080u;
+          uint32_t a[4];
+          a[0] = biased_bytes_to_f16x2(x0, 0x4140);  // token gid,     channels +0, +1
+          a[1] = biased_bytes_to_f16x2(x1, 0x4140);  // token gid + 8
+          a[2] = biased_bytes_to_f16x2(x0, 0x4342);  // token gid,     channels +2, +3
+          a[3] = biased_bytes_to_f16x2(x1, 0x4342);  // token gid + 8
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t x = words[j] ^ 0x80808080u;
-            mma16816<true>(sfr[nt], qa[j], biased_bytes_to_f16x2(x, 0x4140),
-                           biased_bytes_to_f16x2(x, 0x4342));
-          }
+          for (int nt = 0; nt < kNT; ++nt) mma16816<true>(acc[j & 1][nt], a, qb[nt][j][0], qb[nt][j][1]);
         }
       }
 
-      // ---- online softmax (base 2) over this warp's 16 tokens ---------------------
+      // ---- online softmax (base 2) per head over this warp's 16 tokens ---------------
       const float* kscale = reinterpret_cast<const float*>(st + 2 * L::KV_BYTES);
       const float* vscale = kscale + kChunk;
-      float p[2][4];
-      float alpha[2];
-#pragma unroll
-      for (int hr = 0; hr < (kRows16 ? 2 : 1); ++hr) {
-        float x[4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int tok = t0 + 8 * nt + 2 * tig + e;
-            float v = sfr[nt][2 * hr + e] * q_scale;
-            if constexpr (kQuant) v *= kscale[tok];
-            x[2 * nt + e] = tok < valid ? v : -CUDART_INF_F;
-          }
-        }
-        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run[hr], mx);
-        if (m_new == -CUDART_INF_F) {
-          alpha[hr] = 1.f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) p[hr][i] = 0.f;
-        } else {
-          alpha[hr] = exp2f(m_run[hr] - m_new);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) p[hr][i] = exp2f(x[i] - m_new);
-        }
-        l_part[hr] = l_part[hr] * alpha[hr] + (p[hr][0] + p[hr][1]) + (p[hr][2] + p[hr][3]);
-        m_run[hr] = m_new;
-      }
-      if (!kRows16) {
-        alpha[1] = 1.f;
-        p[1][0] = p[1][1] = p[1][2] = p[1][3] = 0.f;
-      }
-      if (alpha[0] != 1.f || alpha[1] != 1.f) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          o[j][0] *= alpha[0];
-          o[j][1] *= alpha[0];
-          o[j][2] *= alpha[1];
-          o[j][3] *= alpha[1];
-        }
-      }
-
-      // ---- O += P V ----------------------------------------------------------------
-      uint32_t pa[4];
+      const int tok_a = t0 + gid, tok_b = t0 + gid + 8;
+      float ks_a = 1.f, ks_b = 1.f, vs_a = 0.f, vs_b = 0.f;
       if constexpr (kQuant) {
-        float vs[4];
+        ks_a = kscale[tok_a];
+        ks_b = kscale[tok_b];
+        vs_a = tok_a < valid ? vscale[tok_a] : 0.f;
+        vs_b = tok_b < valid ? vscale[tok_b] : 0.f;
+      }
+      uint32_t pb[kNT][2];
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        float x[4];  // (token a, head e0), (a, e1), (b, e0), (b, e1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int tok = t0 + 8 * (i >> 1) + 2 * tig + (i & 1);
-          vs[i] = tok < valid ? vscale[tok] : 0.f;
+          float v = (acc[0][nt][i] + acc[1][nt][i]) * q_scale;
+          if constexpr (kQuant) v *= (i < 2 ? ks_a : ks_b);
+          x[i] = (i < 2 ? tok_a : tok_b) < valid ? v : -CUDART_INF_F;
         }
-        pa[0] = pack_f16(p[0][0] * vs[0], p[0][1] * vs[1]);
-        pa[1] = pack_f16(p[1][0] * vs[0], p[1][1] * vs[1]);
-        pa[2] = pack_f16(p[0][2] * vs[2], p[0][3] * vs[3]);
-        pa[3] = pack_f16(p[1][2] * vs[2], p[1][3] * vs[3]);
-        // V rows t0 + 2tig + {0, 1, 8, 9}, channels 16*gid .. 16*gid + 15
+        float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+        for (int m = 4; m <= 16; m <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, m));
+        }
+        float alpha[2], p[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float m_new = fmaxf(m_run[nt][e], e == 0 ? mx0 : mx1);
+          if (m_new == -CUDART_INF_F) {
+            alpha[e] = 1.f;
+            p[e] = p[2 + e] = 0.f;
+          } else {
+            alpha[e] = exp2f(m_run[nt][e] - m_new);
+            p[e] = exp2f(x[e] - m_new);
+            p[2 + e] = exp2f(x[2 + e] - m_new);
+          }
+          l_part[nt][e] = l_part[nt][e] * alpha[e] + (p[e] + p[2 + e]);
+          m_run[nt][e] = m_new;
+        }
+        if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            o[nt][i][0] *= alpha[0];
+            o[nt][i][1] *= alpha[1];
+            o[nt][i][2] *= alpha[0];
+            o[nt][i][3] *= alpha[1];
+          }
+        }
+        // P^T as the B operand of O^T += V^T P^T: transpose the two 8x8 (token, head)
+        // blocks in registers.
+        uint32_t xa, xb;
+        if constexpr (kQuant) {
+          xa = pack_f16(p[0] * vs_a, p[1] * vs_a);
+          xb = pack_f16(p[2] * vs_b, p[3] * vs_b);
+        } else {
+          xa = pack_bf16(p[0], p[1]);
+          xb = pack_bf16(p[2], p[3]);
+        }
+        pb[nt][0] = movmatrix_trans(xa);
+        pb[nt][1] = movmatrix_trans(xb);
+      }
+
+      // ---- O^T += V^T P^T (M = 16 channels per tile, K = 16 tokens) ----------------------
+      if constexpr (kQuant) {
+        // V rows t0 + 2tig + {0, 1, 8, 9}, channels 16*gid .. 16*gid + 15; M-tile i row
+        // gid is channel 16*gid + 2i, row gid + 8 is channel 16*gid + 2i + 1.
         const int r0 = t0 + 2 * tig;
         const uint4 va = *reinterpret_cast<const uint4*>(st + L::KV_BYTES + swz(r0, gid));
         const uint4 vb = *reinterpret_cast<const uint4*>(st + L::KV_BYTES + swz(r0 + 1, gid));
@@ -480,37 +503,33 @@ __global__ void __launch_bounds__(kThreads, MINB)
           const uint32_t xc = wc[w] ^ 0x80808080u, xd = wd[w] ^ 0x80808080u;
           const uint32_t ab_lo = __byte_perm(xa, xb, 0x5140), ab_hi = __byte_perm(xa, xb, 0x7362);
           const uint32_t cd_lo = __byte_perm(xc, xd, 0x5140), cd_hi = __byte_perm(xc, xd, 0x7362);
-          // n-tile j = 4w + k covers channel 16*gid + j
-          mma16816<true>(o[4 * w + 0], pa, biased_bytes_to_f16x2(ab_lo, 0x4140),
-                         biased_bytes_to_f16x2(cd_lo, 0x4140));
-          mma16816<true>(o[4 * w + 1], pa, biased_bytes_to_f16x2(ab_lo, 0x4342),
-                         biased_bytes_to_f16x2(cd_lo, 0x4342));
-          mma16816<true>(o[4 * w + 2], pa, biased_bytes_to_f16x2(ab_hi, 0x4140),
-                         biased_bytes_to_f16x2(cd_hi, 0x4140));
-          mma16816<true>(o[4 * w + 3], pa, biased_bytes_to_f16x2(ab_hi, 0x4342),
-                         biased_bytes_to_f16x2(cd_hi, 0x4342));
+          uint32_t a_even[4] = {biased_bytes_to_f16x2(ab_lo, 0x4140), biased_bytes_to_f16x2(ab_lo, 0x4342),
+                                biased_bytes_to_f16x2(cd_lo, 0x4140), biased_bytes_to_f16x2(cd_lo, 0x4342)};
+          uint32_t a_odd[4] = {biased_bytes_to_f16x2(ab_hi, 0x4140), biased_bytes_to_f16x2(ab_hi, 0x4342),
+                               biased_bytes_to_f16x2(cd_hi, 0x4140), biased_bytes_to_f16x2(cd_hi, 0x4342)};
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            mma16816<true>(o[nt][2 * w], a_even, pb[nt][0], pb[nt][1]);
+            mma16816<true>(o[nt][2 * w + 1], a_odd, pb[nt][0], pb[nt][1]);
+          }
         }
       } else {
-        pa[0] = pack_bf16(p[0][0], p[0][1]);
-        pa[1] = pack_bf16(p[1][0], p[1][1]);
-        pa[2] = pack_bf16(p[0][2], p[0][3]);
-        pa[3] = pack_bf16(p[1][2], p[1][3]);
+        const int mi = lane >> 3;
+        const int row = t0 + (lane & 7) + 8 * (mi >> 1);
 #pragma unroll
-        for (int dp = 0; dp < 8; ++dp) {  // 16 channels per step: two n-tiles
-          const int mi = lane >> 3;
-          const int row = t0 + (lane & 7) + 8 * (mi & 1);
-          const int chunk = 2 * dp + (mi >> 1);
+        for (int i = 0; i < 8; ++i) {  // channels 16i .. 16i + 15
+          const int chunk = 2 * i + (mi & 1);
           const uint32_t addr = vst + (chunk >> 3) * 8192 + swz(row, chunk & 7);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(addr, b0, b1, b2, b3);
-          mma16816<false>(o[2 * dp], pa, b0, b1);
-          mma16816<false>(o[2 * dp + 1], pa, b2, b3);
+          uint32_t a[4];
+          ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) mma16816<false>(o[nt][i], a, pb[nt][0], pb[nt][1]);
         }
       }
     }
     // this warp is done with the stage; zeroing stores (generic proxy) must be ordered
     // before the TMA (async proxy) refills the buffer
-    if (t0 < valid && valid < t0 + 16) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (t0 < valid && partial) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
   }
@@ -518,19 +537,25 @@ __global__ void __launch_bounds__(kThreads, MINB)
   trigger_dependents();
 
   // ---- merge the four warps' softmax states, write the split's partials -------------
-  float l_row[2];
+  float l_head[kNT][2];
 #pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    float v = l_part[hr];
-    v += __shfl_xor_sync(0xffffffffu, v, 1);
-    v += __shfl_xor_sync(0xffffffffu, v, 2);
-    l_row[hr] = v;
-  }
-  if (tig == 0) {
-    ml_s[(warp * 16 + gid) * 2 + 0] = m_run[0];
-    ml_s[(warp * 16 + gid) * 2 + 1] = l_row[0];
-    ml_s[(warp * 16 + gid + 8) * 2 + 0] = m_run[1];
-    ml_s[(warp * 16 + gid + 8) * 2 + 1] = l_row[1];
+  for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float v = l_part[nt][e];
+#pragma unroll
+      for (int m = 4; m <= 16; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+      l_head[nt][e] = v;
+    }
+  if (gid == 0) {
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int head = 8 * nt + 2 * tig + e;
+        ml_s[(warp * 16 + head) * 2 + 0] = m_run[nt][e];
+        ml_s[(warp * 16 + head) * 2 + 1] = l_head[nt][e];
+      }
   }
   consumer_barrier();
   if (failed || *abort_flag) {
@@ -542,36 +567,37 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
     return;
   }
-  float* red = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][128]
+  float* red = reinterpret_cast<float*>(smem);  // [4 warps][16 heads][128 channels]
 #pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int row = gid + 8 * hr;
-    float mrow = -CUDART_INF_F;
+  for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + row) * 2]);
-    const float scale = m_run[hr] == -CUDART_INF_F ? 0.f : exp2f(m_run[hr] - mrow);
-    float* dst = red + (warp * 16 + row) * 128;
+    for (int e = 0; e < 2; ++e) {
+      const int head = 8 * nt + 2 * tig + e;
+      if (head < G) {
+        float mrow = -CUDART_INF_F;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if constexpr (kQuant) {
-        dst[32 * tig + j] = o[j][2 * hr] * scale;         // channel 16*(2tig) + j
-        dst[32 * tig + 16 + j] = o[j][2 * hr + 1] * scale; // channel 16*(2tig+1) + j
-      } else {
-        *reinterpret_cast<float2*>(dst + 8 * j + 2 * tig) =
-            make_float2(o[j][2 * hr] * scale, o[j][2 * hr + 1] * scale);
+        for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + head) * 2]);
+        const float scale = m_run[nt][e] == -CUDART_INF_F ? 0.f : exp2f(m_run[nt][e] - mrow);
+        float* dst = red + (warp * 16 + head) * 128;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int ch0 = kQuant ? 16 * gid + 2 * i : 16 * i + gid;
+          const int ch1 = kQuant ? 16 * gid + 2 * i + 1 : 16 * i + gid + 8;
+          dst[ch0] = o[nt][i][e] * scale;
+          dst[ch1] = o[nt][i][2 + e] * scale;
+        }
       }
     }
-  }
   consumer_barrier();
   for (int idx = tid; idx < G * 32; idx += kConsumerWarps * 32) {
-    const int row = idx >> 5, d = (idx & 31) * 4;
+    const int head = idx >> 5, d = (idx & 31) * 4;
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float4 v = *reinterpret_cast<const float4*>(red + (w * 16 + row) * 128 + d);
+      const float4 v = *reinterpret_cast<const float4*>(red + (w * 16 + head) * 128 + d);
       sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
     }
-    *reinterpret_cast<float4*>(prm.acc_out + (slot0 + static_cast<int64_t>(row) * S) * 128 + d) =
+    *reinterpret_cast<float4*>(prm.acc_out + (slot0 + static_cast<int64_t>(head) * S) * 128 + d) =
         sum;
   }
   if (tid < G) {
@@ -635,12 +661,12 @@ inline cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, bool quan
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool kQuant, int P, int STAGES, int MINB, bool kRows16>
+template <bool kQuant, int P, int STAGES, int MINB, int kNT>
 cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
                            dim3 grid, cudaStream_t stream, bool use_pdl) {
   using L = Layout<kQuant, STAGES>;
   void (*kernel)(const CUtensorMap, const CUtensorMap, const SplitKParams) =
-      splitk_mma_kernel<kQuant, P, STAGES, MINB, kRows16>;
+      splitk_mma_kernel<kQuant, P, STAGES, MINB, kNT>;
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -655,7 +681,9 @@ cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const C
                        use_pdl, mk, mv, p);
 }
 
-template <bool kQuant, int STAGES, int MINB>
+// (STAGES, MINB) for G <= 8 (one n-tile of heads) and for G = 16 (two n-tiles, more
+// registers per thread).
+template <bool kQuant, int STAGES1, int MINB1, int STAGES2, int MINB2>
 cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_size,
                             cudaStream_t stream, bool use_pdl) {
   CUtensorMap mk, mv;
@@ -665,13 +693,12 @@ cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_s
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(p.num_splits), static_cast<unsigned>(p.num_kv_heads),
                   static_cast<unsigned>(bs));
-  const bool rows16 = group > 8;
-#define PA_MMA_CASE(PP)                                                                     \
-  if (page_size == PP) {                                                                    \
-    return rows16 ? launch_mma_one<kQuant, PP, STAGES, MINB, true>(p, mk, mv, grid, stream, \
-                                                                   use_pdl)                 \
-                  : launch_mma_one<kQuant, PP, STAGES, MINB, false>(p, mk, mv, grid, stream, \
-                                                                    use_pdl);               \
+  const bool two_tiles = group > 8;
+#define PA_MMA_CASE(PP)                                                                        \
+  if (page_size == PP) {                                                                       \
+    return two_tiles                                                                           \
+               ? launch_mma_one<kQuant, PP, STAGES2, MINB2, 2>(p, mk, mv, grid, stream, use_pdl) \
+               : launch_mma_one<kQuant, PP, STAGES1, MINB1, 1>(p, mk, mv, grid, stream, use_pdl); \
   }
   PA_MMA_CASE(16)
   PA_MMA_CASE(32)

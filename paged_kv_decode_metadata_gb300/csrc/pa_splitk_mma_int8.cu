@@ -3,11 +3,19 @@
 
 namespace pa {
 
-// Six 17 KiB stages per CTA (codes and scales of a 64-token chunk), two CTAs per SM:
-// the int8 widening needs more registers than three CTAs per SM leave.
+#ifndef PA_MMA_INT8_STAGES1
+// G <= 8: four 17 KiB stages (codes and scales of a 64-token chunk) per CTA, three CTAs
+// per SM.  G = 16: six stages, two CTAs per SM.
+#define PA_MMA_INT8_STAGES1 4
+#define PA_MMA_INT8_MINB1 3
+#define PA_MMA_INT8_STAGES2 6
+#define PA_MMA_INT8_MINB2 2
+#endif
+
 cudaError_t launch_splitk_mma_int8(const SplitKParams& p, int bs, int group, int page_size,
                                    cudaStream_t stream, bool use_pdl) {
-  return mma::launch_mma_impl<true, 6, 2>(p, bs, group, page_size, stream, use_pdl);
+  return mma::launch_mma_impl<true, PA_MMA_INT8_STAGES1, PA_MMA_INT8_MINB1, PA_MMA_INT8_STAGES2,
+                              PA_MMA_INT8_MINB2>(p, bs, group, page_size, stream, use_pdl);
 }
 
 }  // namespace pa
