@@ -273,6 +273,54 @@ def pdl_study(torch, synthetic, DeviceStep, stream, replays=3000):
     return out
 
 
+def pdl_gap_study(torch, synthetic, DeviceStep, binding, stream, reps=300):
+    """Inter-stage gaps of one decode step from the timestamp-instrumented build: each
+    kernel records its earliest block entry, earliest return from griddepcontrol.wait
+    and latest warp finish (%globaltimer).  One step at a time, graph replay, with and
+    without PDL; medians over `reps` steps, nanoseconds."""
+    import numpy as np
+
+    lib = binding.load_instrumented()
+    buf = torch.empty(9, dtype=torch.int64, device="cuda")
+    init = torch.tensor([-1, -1, 0] * 3, dtype=torch.int64, device="cuda")  # UINT64_MAX / 0
+    if lib.pa_set_timestamp_buffer(buf.data_ptr()) != 0:
+        raise RuntimeError("pa_set_timestamp_buffer failed")
+    result = {}
+    try:
+        for name in ("bs1_ctx1k", "bs1_ctx8k"):
+            wl = synthetic.make(synthetic.WORKLOADS[name])
+            ds = DeviceStep(wl)
+            row = {}
+            for pdl in (False, True):
+                g = capture(torch, lambda: ds.step(use_pdl=pdl, lib=lib), stream)
+                rec = []
+                for _ in range(reps):
+                    with torch.cuda.stream(stream):
+                        buf.copy_(init)
+                        g.replay()
+                    stream.synchronize()
+                    rec.append(buf.cpu().numpy().view(np.uint64).astype(np.float64))
+                del g
+                r = np.median(np.stack(rec), axis=0)
+                e0, w0, x0, e1, w1, x1, e2, w2, x2 = r
+                key = "pdl" if pdl else "no_pdl"
+                row[key] = {
+                    "step_ns": x2 - e0,
+                    "metadata_ns": x0 - e0,
+                    "producer_ns": x1 - w1,
+                    "reducer_ns": x2 - w2,
+                    "gap_metadata_to_producer_ns": w1 - x0,
+                    "gap_producer_to_reducer_ns": w2 - x1,
+                    "producer_resident_before_metadata_end_ns": x0 - e1,
+                    "reducer_resident_before_producer_end_ns": x1 - e2,
+                }
+            result[name] = row
+            del ds
+    finally:
+        lib.pa_set_timestamp_buffer(None)
+    return result
+
+
 def run_gb300(args, spec, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -283,6 +331,8 @@ def run_gb300(args, spec, rank, world, local_rank):
 
     if rank == 0:
         pa_build.build()
+        if not args.no_extras:
+            pa_build.build(instrumented=True)
     if world > 1:
         dist.barrier()
     torch.cuda.set_device(local_rank)
@@ -394,6 +444,7 @@ def run_gb300(args, spec, rank, world, local_rank):
         extras["graph_no_pdl_us"] = time_graph(torch, g_nopdl, min(args.steps, 2000), stream)
         del g_nopdl
         extras["pdl_bs1"] = pdl_study(torch, synthetic, DeviceStep, stream)
+        extras["pdl_gaps_bs1"] = pdl_gap_study(torch, synthetic, DeviceStep, binding, stream)
         extras["cpu_baseline"] = cpu_baseline(wl)
 
     flags = binding.pa_read_error_flags(reset=True)

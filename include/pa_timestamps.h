@@ -1,0 +1,36 @@
+/*
+ * pa_timestamps.h -- extra entry point of the instrumented build (libpa_ts.so).
+ *
+ * The instrumented build is the same library compiled with -DPA_TIMESTAMPS: every
+ * kernel records %globaltimer nanoseconds into a caller-owned device buffer, so the
+ * gaps between the three stages of a decode step (and how much of them PDL hides)
+ * can be measured without a tracing tool.  The production libpa.so does not export
+ * this call and its kernels carry none of the instrumentation.
+ */
+#ifndef PA_TIMESTAMPS_H_
+#define PA_TIMESTAMPS_H_
+
+#include <stdint.h>
+
+#include "pa.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Make later launches record stage times into `buffer` (device memory, 9 uint64,
+ * NULL stops recording).  Stage k = 0 metadata, 1 split-K producer, 2 reducer:
+ *   buffer[3k + 0]  earliest block entry            (atomicMin; preset to UINT64_MAX)
+ *   buffer[3k + 1]  earliest return from the wait on the previous grid (atomicMin)
+ *   buffer[3k + 2]  latest warp finish              (atomicMax; preset to 0)
+ * The buffer pointer is captured into kernel arguments at launch (and so into CUDA
+ * graphs captured afterwards).  The caller resets the buffer between steps.
+ */
+pa_status pa_set_timestamp_buffer(uint64_t* buffer);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_TIMESTAMPS_H_ */

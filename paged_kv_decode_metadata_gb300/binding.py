@@ -57,6 +57,26 @@ def load() -> ctypes.CDLL:
     return _lib
 
 
+_ts_lib: Optional[ctypes.CDLL] = None
+
+
+def load_instrumented() -> ctypes.CDLL:
+    """Load the timestamp-instrumented build ``_build/libpa_ts.so`` (same entry points
+    plus pa_set_timestamp_buffer, include/pa_timestamps.h); raise if it is missing."""
+    global _ts_lib
+    with _lock:
+        if _ts_lib is None:
+            path = _build.TS_LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(f"instrumented library {path} is missing; build it with "
+                                   "`python -m paged_kv_decode_metadata_gb300.build --ts`")
+            lib = _declare(ctypes.CDLL(path))
+            lib.pa_set_timestamp_buffer.argtypes = [ctypes.c_void_p]
+            lib.pa_set_timestamp_buffer.restype = ctypes.c_int
+            _ts_lib = lib
+    return _ts_lib
+
+
 def _declare(lib):
     vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                              ctypes.c_size_t)
@@ -228,9 +248,10 @@ def pa_decode_step(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: i
                    max_seq_pages: int, cache_seqlens, cu_seqlens_k, page_table, q, k_cache,
                    v_cache, num_splits: int, sm_scale: float, workspace, out, lse=None,
                    k_scale=None, v_scale=None, full_to_swa_mapping=None, swa_page_table=None,
-                   stream=None, use_pdl: bool = True):
-    """Metadata + split-K producer + reducer in one call; see include/pa.h."""
-    lib = load()
+                   stream=None, use_pdl: bool = True, lib=None):
+    """Metadata + split-K producer + reducer in one call; see include/pa.h.  ``lib``
+    selects another build of the library (e.g. ``load_instrumented()``)."""
+    lib = lib or load()
     kv_dtype, ks, vs = _kv_args(k_cache, v_cache, k_scale, v_scale)
     bs, hq, d = q.shape
     num_pages, hkv, page_size, _ = k_cache.shape

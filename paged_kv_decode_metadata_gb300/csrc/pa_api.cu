@@ -18,6 +18,8 @@ __device__ unsigned int g_pa_error_flags;
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned int*> g_err_ptr[kMaxDevices];
 std::atomic<int32_t> g_producer{PA_PRODUCER_AUTO};
+// Stage timestamp buffer (9 uint64) of the instrumented build; nullptr otherwise.
+std::atomic<unsigned long long*> g_ts{nullptr};
 std::atomic<int> g_sm_count[kMaxDevices];
 
 cudaError_t error_word(unsigned int** out) {
@@ -175,6 +177,7 @@ pa_status pa_build_metadata_full(
   p.page_size = page_size;
   p.q_mode = q_mode;
   p.q_stride = q_stride;
+  p.ts = g_ts.load();
   cudaError_t e = error_word(&p.err);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   return launch_metadata_checked(p, static_cast<cudaStream_t>(stream), use_pdl);
@@ -235,6 +238,7 @@ pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cac
   p.m_out = scratch_m;
   p.l_out = scratch_l;
   p.acc_out = scratch_acc;
+  p.ts = g_ts.load();
   cudaError_t e = error_word(&p.err);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -266,6 +270,7 @@ pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const float*
   p.num_splits = num_splits;
   p.out = out;
   p.lse = lse;
+  p.ts = g_ts.load();
   cudaError_t e = pa::launch_reduce(p, static_cast<cudaStream_t>(stream), use_pdl != 0);
   if (e == cudaSuccess) e = cudaGetLastError();
   return from_cuda(e);
@@ -349,6 +354,14 @@ pa_status pa_decode_step(
   if (st != PA_OK) return st;
   return pa_reduce(m, l, acc, bs, num_q_heads, head_dim, splits, out, lse, stream, use_pdl);
 }
+
+#ifdef PA_TIMESTAMPS
+// Instrumented build only (include/pa_timestamps.h).
+pa_status pa_set_timestamp_buffer(uint64_t* buffer) {
+  g_ts.store(reinterpret_cast<unsigned long long*>(buffer));
+  return PA_OK;
+}
+#endif
 
 int32_t pa_select_producer(int32_t producer) {
   if (producer != PA_PRODUCER_AUTO && producer != PA_PRODUCER_FMA && producer != PA_PRODUCER_MMA)

@@ -107,6 +107,27 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Stage timestamps for measuring launch gaps (builds with -DPA_TIMESTAMPS only; the
+// production build compiles these to nothing).  Stage k (0 metadata, 1 producer,
+// 2 reducer) owns slots 3k: earliest block entry, 3k+1: earliest pass of
+// griddepcontrol.wait, 3k+2: latest warp finish, all %globaltimer nanoseconds.
+enum : int { kTsEntry = 0, kTsReady = 1, kTsExit = 2 };
+#ifdef PA_TIMESTAMPS
+#define PA_TS_FIRST(ts, stage, what)                                                      \
+  do {                                                                                   \
+    if ((ts) != nullptr && threadIdx.x == 0)                                             \
+      atomicMin((ts) + 3 * (stage) + (what), ::pa::global_timer_ns());                   \
+  } while (0)
+#define PA_TS_LAST(ts, stage)                                                             \
+  do {                                                                                   \
+    if ((ts) != nullptr && (threadIdx.x & 31) == 0)                                      \
+      atomicMax((ts) + 3 * (stage) + ::pa::kTsExit, ::pa::global_timer_ns());            \
+  } while (0)
+#else
+#define PA_TS_FIRST(ts, stage, what) ((void)0)
+#define PA_TS_LAST(ts, stage) ((void)0)
+#endif
+
 __device__ __forceinline__ void record_error(unsigned int* err, unsigned int bit) {
   if (err != nullptr) atomicOr(err, bit);
 }

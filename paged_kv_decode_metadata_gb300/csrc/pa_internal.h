@@ -33,6 +33,7 @@ struct MetadataParams {
   int32_t q_mode;
   int32_t q_stride;
   unsigned int* err;
+  unsigned long long* ts;  // stage timestamps (instrumented builds only), else nullptr
 };
 
 struct SplitKParams {
@@ -55,6 +56,7 @@ struct SplitKParams {
   float* l_out;
   float* acc_out;
   unsigned int* err;
+  unsigned long long* ts;  // stage timestamps (instrumented builds only), else nullptr
 };
 
 struct ReduceParams {
@@ -65,6 +67,7 @@ struct ReduceParams {
   int32_t num_splits;
   void* out;   // bf16 [num_rows, 128]
   float* lse;  // [num_rows] or nullptr
+  unsigned long long* ts;  // stage timestamps (instrumented builds only), else nullptr
 };
 
 cudaError_t launch_metadata(const MetadataParams& p, cudaStream_t stream, bool use_pdl);

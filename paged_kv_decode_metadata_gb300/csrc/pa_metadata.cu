@@ -52,7 +52,9 @@ __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* w
 }
 
 __global__ void __launch_bounds__(kThreads) metadata_kernel(const MetadataParams p) {
+  PA_TS_FIRST(p.ts, 0, kTsEntry);
   grid_dependency_wait();
+  PA_TS_FIRST(p.ts, 0, kTsReady);
   trigger_dependents();
 
   const int tid = threadIdx.x;
@@ -92,6 +94,7 @@ __global__ void __launch_bounds__(kThreads) metadata_kernel(const MetadataParams
         swa_out[col] = swa_token < 0 ? -1 : static_cast<int32_t>(swa_token / p.page_size);
       }
     }
+    PA_TS_LAST(p.ts, 0);
     return;
   }
 
@@ -128,12 +131,16 @@ __global__ void __launch_bounds__(kThreads) metadata_kernel(const MetadataParams
       }
       if (tid == 0) p.cu_seqlens_q[0] = 0;
     }
+    PA_TS_LAST(p.ts, 0);
     return;
   }
 
   // ---- swa_out_cache_loc tile ------------------------------------------------------
   const int64_t idx = static_cast<int64_t>(blk - p.bs - 1) * kThreads + tid;
-  if (idx >= p.swa_out_len) return;
+  if (idx >= p.swa_out_len) {
+    PA_TS_LAST(p.ts, 0);
+    return;
+  }
   int64_t value = 0;
   if (idx < p.num_out_tokens) {
     const int64_t loc = p.out_cache_loc[idx];
@@ -147,6 +154,7 @@ __global__ void __launch_bounds__(kThreads) metadata_kernel(const MetadataParams
     }
   }
   p.swa_out_cache_loc[idx] = value;
+  PA_TS_LAST(p.ts, 0);
 }
 
 }  // namespace

@@ -29,8 +29,13 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceParams p) 
   const int S = p.num_splits;
   float* w = weights + warp * S;
 
+  PA_TS_FIRST(p.ts, 2, kTsEntry);
   grid_dependency_wait();  // the producer's partials are complete and visible
-  if (row >= p.num_rows) return;
+  PA_TS_FIRST(p.ts, 2, kTsReady);
+  if (row >= p.num_rows) {
+    PA_TS_LAST(p.ts, 2);
+    return;
+  }
 
   const float* m = p.m + row * S;
   const float* l = p.l + row * S;
@@ -43,6 +48,7 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceParams p) 
     trigger_dependents();
     *reinterpret_cast<uint2*>(out) = make_uint2(0u, 0u);
     if (p.lse != nullptr && lane == 0) p.lse[row] = -CUDART_INF_F;
+    PA_TS_LAST(p.ts, 2);
     return;
   }
 
@@ -78,6 +84,7 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceParams p) 
   packed.y = *reinterpret_cast<const uint32_t*>(&hi);
   *reinterpret_cast<uint2*>(out) = packed;
   if (p.lse != nullptr && lane == 0) p.lse[row] = mx + logf(total);
+  PA_TS_LAST(p.ts, 2);
 }
 
 }  // namespace

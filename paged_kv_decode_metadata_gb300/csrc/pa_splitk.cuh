@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(128, MINB) splitk_kernel(const SplitKParams pr
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rg = tid / LPR, r = tid % LPR;
   const int num_splits = prm.num_splits;
+  PA_TS_FIRST(prm.ts, 1, kTsEntry);
 
   // ---- prologue that does not depend on the metadata stage: the query rows -------
   float qf[G][E];
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(128, MINB) splitk_kernel(const SplitKParams pr
 
   // ---- everything below reads what the metadata stage wrote ----------------------
   grid_dependency_wait();
+  PA_TS_FIRST(prm.ts, 1, kTsReady);
 
   int n = prm.cache_seqlens[b];
   const int cap = prm.max_seq_pages * P;
@@ -180,6 +182,7 @@ __global__ void __launch_bounds__(128, MINB) splitk_kernel(const SplitKParams pr
       prm.m_out[slot0 + static_cast<int64_t>(tid) * num_splits] = -CUDART_INF_F;
       prm.l_out[slot0 + static_cast<int64_t>(tid) * num_splits] = 0.f;
     }
+    PA_TS_LAST(prm.ts, 1);
     return;
   }
 
@@ -445,6 +448,7 @@ __global__ void __launch_bounds__(128, MINB) splitk_kernel(const SplitKParams pr
       prm.l_out[slot] = l_run[j];
     }
   }
+  PA_TS_LAST(prm.ts, 1);
 }
 
 // Host launch of one instantiation.  The dynamic shared-memory limit is raised once

@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const int G = prm.num_q_heads / prm.num_kv_heads;
   const int S = prm.num_splits;
   const bool is_consumer = warp < kConsumerWarps;
+  PA_TS_FIRST(prm.ts, 1, kTsEntry);
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_FULL);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L::OFF_EMPTY);
@@ -213,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
   // ---- everything below reads what the metadata stage wrote -------------------------
   grid_dependency_wait();
+  PA_TS_FIRST(prm.ts, 1, kTsReady);
 
   int n = prm.cache_seqlens[b];
   const int cap = prm.max_seq_pages * P;
@@ -234,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       prm.m_out[slot0 + static_cast<int64_t>(tid) * S] = -CUDART_INF_F;
       prm.l_out[slot0 + static_cast<int64_t>(tid) * S] = 0.f;
     }
+    PA_TS_LAST(prm.ts, 1);
     return;
   }
 
@@ -613,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     prm.m_out[slot0 + static_cast<int64_t>(tid) * S] = mrow * 0.69314718055994530942f;
     prm.l_out[slot0 + static_cast<int64_t>(tid) * S] = lsum;
   }
+  PA_TS_LAST(prm.ts, 1);
 }
 
 // ---- host side ------------------------------------------------------------------------

@@ -82,7 +82,7 @@ class DeviceStep:
         self.splitk(use_pdl, stream)
         self.reduce(use_pdl, stream)
 
-    def step(self, use_pdl=True, stream=None):
+    def step(self, use_pdl=True, stream=None, lib=None):
         B.pa_decode_step(req_pool_indices=self.req_pool_indices, seq_lens=self.seq_lens,
                          req_to_token=self.req_to_token, seqlen_offset=self.seqlen_offset,
                          max_seq_pages=self.max_seq_pages, cache_seqlens=self.cache_seqlens,
@@ -91,7 +91,8 @@ class DeviceStep:
                          sm_scale=self.sm_scale, workspace=self.workspace, out=self.out,
                          lse=self.lse, k_scale=self.k_scale, v_scale=self.v_scale,
                          full_to_swa_mapping=self.full_to_swa_mapping,
-                         swa_page_table=self.swa_page_table, stream=stream, use_pdl=use_pdl)
+                         swa_page_table=self.swa_page_table, stream=stream, use_pdl=use_pdl,
+                         lib=lib)
 
     # ---- accounting -----------------------------------------------------------------
     def kv_bytes(self, ctx) -> int:

@@ -97,3 +97,18 @@ def test_workspace_and_split_heuristic(lib):
         assert -(-pages // pps) == s          # the longest request has no empty split
     assert B.pa_choose_splits(0, 8, 16, 64, 152) == 1
     assert B.pa_status_string(B.PA_ERR_UNSUPPORTED) == "unsupported shape"
+
+
+TS_HEADER = os.path.join(os.path.dirname(HEADER), "pa_timestamps.h")
+
+
+def test_instrumented_build_exports_its_header_and_production_does_not():
+    build.build(instrumented=True)
+    ts = B.load_instrumented()
+    text = re.sub(r"/\*.*?\*/", "", open(TS_HEADER).read(), flags=re.S)
+    names = sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+    assert names == ["pa_set_timestamp_buffer"]
+    for n in names + declared_functions():
+        assert hasattr(ts, n), n
+    prod = ctypes.CDLL(build.LIB_PATH)
+    assert not hasattr(prod, "pa_set_timestamp_buffer")
