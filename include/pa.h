@@ -38,6 +38,11 @@
 extern "C" {
 #endif
 
+/* Only the entry points below are exported from the shared library. */
+#ifndef PA_API
+#define PA_API __attribute__((visibility("default")))
+#endif
+
 typedef enum {
   PA_OK = 0,
   PA_ERR_INVALID = 1,
@@ -100,7 +105,7 @@ typedef enum {
  *   req_to_token_stride when max_seq_pages > 0.
  * Errors: PA_ERR_INVALID as listed in the file comment.
  */
-pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_t* seq_lens,
+PA_API pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_t* seq_lens,
                             const int32_t* req_to_token, int64_t req_to_token_rows,
                             int64_t req_to_token_stride,
                             const int64_t* full_to_swa_mapping,
@@ -122,7 +127,7 @@ pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_t* seq_
  *   num_out_tokens = min(swa_out_len, out_cache_loc_len)
  * swa_out_cache_loc [swa_out_len] int64 (out) or NULL; it needs the mapping.
  */
-pa_status pa_build_metadata_full(
+PA_API pa_status pa_build_metadata_full(
     const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
     int64_t req_to_token_rows, int64_t req_to_token_stride,
     const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
@@ -167,7 +172,7 @@ pa_status pa_build_metadata_full(
  * With use_pdl, q is read before the kernel waits on the previous grid (the prologue
  * overlaps the metadata stage): the kernel launched just before must not write q.
  */
-pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
+PA_API pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
                            const float* k_scale, const float* v_scale, int32_t kv_dtype,
                            const int32_t* page_table, int64_t page_table_stride,
                            const int32_t* cache_seqlens, int32_t bs, int32_t num_q_heads,
@@ -187,7 +192,7 @@ pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cac
  *   out [bs, num_q_heads, head_dim] bf16; lse [bs, num_q_heads] fp32 or NULL.
  * Supported: head_dim 128.
  */
-pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const float* scratch_acc,
+PA_API pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const float* scratch_acc,
                     int32_t bs, int32_t num_q_heads, int32_t head_dim, int32_t num_splits,
                     void* out, float* lse, void* stream, int32_t use_pdl);
 
@@ -200,7 +205,7 @@ pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const float*
  * num_splits, or pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, 0)
  * when num_splits == 0.
  */
-pa_status pa_decode_step(
+PA_API pa_status pa_decode_step(
     const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
     int64_t req_to_token_rows, int64_t req_to_token_stride,
     const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
@@ -237,7 +242,7 @@ pa_status pa_decode_step(
  */
 #define PA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
-pa_status pa_decode_step_static_scratch(
+PA_API pa_status pa_decode_step_static_scratch(
     const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
     int64_t req_to_token_rows, int64_t req_to_token_stride,
     const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
@@ -250,7 +255,7 @@ pa_status pa_decode_step_static_scratch(
     float sm_scale, void* out, float* lse, void* stream, int32_t use_pdl);
 
 /* Bytes of workspace pa_decode_step needs: m, l and acc partials, each 256-byte aligned. */
-size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim,
+PA_API size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim,
                           int32_t num_splits);
 
 /*
@@ -259,7 +264,7 @@ size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim,
  * longest request with an empty split.  sm_count <= 0 queries the current device.
  * Returns >= 1 (1 for degenerate sizes).
  */
-int32_t pa_choose_splits(int32_t bs, int32_t num_kv_heads, int32_t max_seq_pages,
+PA_API int32_t pa_choose_splits(int32_t bs, int32_t num_kv_heads, int32_t max_seq_pages,
                          int32_t page_size, int32_t sm_count);
 
 /*
@@ -267,16 +272,23 @@ int32_t pa_choose_splits(int32_t bs, int32_t num_kv_heads, int32_t max_seq_pages
  * (PA_PRODUCER_AUTO, _FMA or _MMA); returns the previous choice.  An unknown value
  * changes nothing and returns the current choice.  Meant for A/B measurement.
  */
-int32_t pa_select_producer(int32_t producer);
+PA_API int32_t pa_select_producer(int32_t producer);
+
+/*
+ * Description of the last CUDA failure an entry point saw on the calling host thread
+ * (the call that failed and the CUDA error), or "no CUDA error".  The string stays
+ * valid until the next failing call on that thread.
+ */
+PA_API const char* pa_last_error_string(void);
 
 /* Static description of a status code. */
-const char* pa_status_string(pa_status status);
+PA_API const char* pa_status_string(pa_status status);
 
 /*
  * Read (and, when reset != 0, clear) the current device's error word.  This call
  * synchronises the device; it is for tests and diagnostics, not the hot path.
  */
-pa_status pa_read_error_flags(uint32_t* flags, int32_t reset);
+PA_API pa_status pa_read_error_flags(uint32_t* flags, int32_t reset);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,7 @@ extern "C" {
  * The buffer pointer is captured into kernel arguments at launch (and so into CUDA
  * graphs captured afterwards).  The caller resets the buffer between steps.
  */
-pa_status pa_set_timestamp_buffer(uint64_t* buffer);
+PA_API pa_status pa_set_timestamp_buffer(uint64_t* buffer);
 
 #ifdef __cplusplus
 }

@@ -33,9 +33,12 @@ _lib: Optional[ctypes.CDLL] = None
 
 
 class PAError(RuntimeError):
-    def __init__(self, func: str, status: int):
+    def __init__(self, func: str, status: int, lib=None):
         self.status = status
-        super().__init__(f"{func} failed: {status_string(status)} ({status})")
+        detail = ""
+        if status == PA_ERR_CUDA:
+            detail = ": " + (lib or load()).pa_last_error_string().decode()
+        super().__init__(f"{func} failed: {status_string(status)} ({status}){detail}")
 
 
 def library_path() -> str:
@@ -102,6 +105,8 @@ def _declare(lib):
     lib.pa_choose_splits.restype = i32
     lib.pa_select_producer.argtypes = [i32]
     lib.pa_select_producer.restype = i32
+    lib.pa_last_error_string.argtypes = []
+    lib.pa_last_error_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [i32]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_read_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
@@ -115,9 +120,9 @@ def status_string(status: int) -> str:
     return load().pa_status_string(int(status)).decode()
 
 
-def _check(func: str, status: int):
+def _check(func: str, status: int, lib=None):
     if status != PA_OK:
-        raise PAError(func, status)
+        raise PAError(func, status, lib)
 
 
 def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
@@ -271,7 +276,7 @@ def pa_decode_step(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: i
         int(num_splits), float(sm_scale), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _ptr(out, torch.bfloat16, "out"),
         _ptr(lse, torch.float32, "lse"), _stream(stream), int(bool(use_pdl)))
-    _check("pa_decode_step", st)
+    _check("pa_decode_step", st, lib)
 
 
 def pa_decode_step_static_scratch(*, req_pool_indices, seq_lens, req_to_token,

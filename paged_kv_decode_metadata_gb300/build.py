@@ -26,8 +26,14 @@ LIB_PATH = os.path.join(BUILD_DIR, "libpa.so")
 TS_LIB_PATH = os.path.join(BUILD_DIR, "libpa_ts.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# Hidden visibility: the library exports only the C ABI (PA_API in include/pa.h).  Two
+# builds loaded in one process (production and instrumented) then share no symbol --
+# function-local statics of templates would otherwise be unified across libraries.
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-              "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]
+              "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",
+              f"-I{INCLUDE}", f"-I{CSRC}"]
+# Keep the statically linked CUDA runtime's symbols local to the library.
+LINK_FLAGS = ["-Xlinker", "--exclude-libs,ALL"]
 
 
 def _nvcc() -> str:
@@ -76,7 +82,7 @@ def build(force: bool = False, verbose_ptxas: bool = False, instrumented: bool =
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra, obj_dir), srcs))
     tmp = lib_path + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
+    cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", *LINK_FLAGS, *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

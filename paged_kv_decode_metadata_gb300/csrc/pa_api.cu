@@ -5,8 +5,10 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 
 #include "../../include/pa.h"
+#include "../../include/pa_timestamps.h"
 #include "pa_internal.h"
 
 namespace {
@@ -52,7 +54,16 @@ int sm_count_of_current_device() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+// Last CUDA failure seen by an entry point on this host thread (pa_last_error_string).
+thread_local char g_last_error[256] = "no CUDA error";
+
+pa_status from_cuda(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return PA_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "%s [%s]: %s (%s)", where, pa::g_fail_site,
+           cudaGetErrorString(e), cudaGetErrorName(e));
+  pa::g_fail_site = "launch";
+  return PA_ERR_CUDA;
+}
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -117,7 +128,7 @@ pa_status launch_metadata_checked(const pa::MetadataParams& p, cudaStream_t stre
                                   int32_t use_pdl) {
   cudaError_t e = pa::launch_metadata(p, stream, use_pdl != 0);
   if (e == cudaSuccess) e = cudaGetLastError();
-  return from_cuda(e);
+  return from_cuda(e, "metadata launch");
 }
 
 }  // namespace
@@ -179,7 +190,7 @@ pa_status pa_build_metadata_full(
   p.q_stride = q_stride;
   p.ts = g_ts.load();
   cudaError_t e = error_word(&p.err);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return from_cuda(e, "error word lookup");
   return launch_metadata_checked(p, static_cast<cudaStream_t>(stream), use_pdl);
 }
 
@@ -240,7 +251,7 @@ pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cac
   p.acc_out = scratch_acc;
   p.ts = g_ts.load();
   cudaError_t e = error_word(&p.err);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return from_cuda(e, "error word lookup");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (kv_dtype == PA_KV_INT8) {
     e = use_fma ? pa::launch_splitk_int8(p, bs, group, page_size, s, use_pdl != 0)
@@ -249,8 +260,8 @@ pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cac
     e = use_fma ? pa::launch_splitk_bf16(p, bs, group, page_size, s, use_pdl != 0)
                 : pa::launch_splitk_mma_bf16(p, bs, group, page_size, s, use_pdl != 0);
   }
-  if (e == cudaSuccess) e = cudaGetLastError();
-  return from_cuda(e);
+  if (e == cudaSuccess) e = pa::fail_at(cudaGetLastError(), "error state after launch");
+  return from_cuda(e, "split-K producer launch");
 }
 
 pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const float* scratch_acc,
@@ -273,7 +284,7 @@ pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const float*
   p.ts = g_ts.load();
   cudaError_t e = pa::launch_reduce(p, static_cast<cudaStream_t>(stream), use_pdl != 0);
   if (e == cudaSuccess) e = cudaGetLastError();
-  return from_cuda(e);
+  return from_cuda(e, "reducer launch");
 }
 
 size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim,
@@ -383,17 +394,19 @@ const char* pa_status_string(pa_status status) {
 pa_status pa_read_error_flags(uint32_t* flags, int32_t reset) {
   if (flags == nullptr) return PA_ERR_INVALID;
   cudaError_t e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return from_cuda(e, "cudaDeviceSynchronize");
   unsigned int v = 0;
   e = cudaMemcpyFromSymbol(&v, g_pa_error_flags, sizeof(v));
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return from_cuda(e, "error word read");
   *flags = v;
   if (reset) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(g_pa_error_flags, &zero, sizeof(zero));
-    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (e != cudaSuccess) return from_cuda(e, "error word reset");
   }
   return PA_OK;
 }
+
+const char* pa_last_error_string(void) { return g_last_error; }
 
 }  // extern "C"

@@ -70,6 +70,13 @@ struct ReduceParams {
   unsigned long long* ts;  // stage timestamps (instrumented builds only), else nullptr
 };
 
+// Step of the last failed launch on this host thread (for pa_last_error_string).
+inline thread_local const char* g_fail_site = "launch";
+inline cudaError_t fail_at(cudaError_t e, const char* site) {
+  if (e != cudaSuccess) g_fail_site = site;
+  return e;
+}
+
 cudaError_t launch_metadata(const MetadataParams& p, cudaStream_t stream, bool use_pdl);
 
 // bs, grid and shapes are validated by the caller.

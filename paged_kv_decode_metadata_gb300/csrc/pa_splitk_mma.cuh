@@ -678,11 +678,12 @@ cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const C
   const unsigned long long bit = 1ull << (dev & 63);
   if ((configured.load() & bit) == 0) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return fail_at(e, "shared-memory attribute");
     configured.fetch_or(bit);
   }
-  return launch_kernel(kernel, grid, dim3(kThreads), static_cast<size_t>(L::SMEM), stream,
-                       use_pdl, mk, mv, p);
+  return fail_at(launch_kernel(kernel, grid, dim3(kThreads), static_cast<size_t>(L::SMEM), stream,
+                               use_pdl, mk, mv, p),
+                 "cudaLaunchKernelEx");
 }
 
 // (STAGES, MINB) for G <= 8 (one n-tile of heads) and for G = 16 (two n-tiles, more
@@ -692,9 +693,9 @@ cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_s
                             cudaStream_t stream, bool use_pdl) {
   CUtensorMap mk, mv;
   cudaError_t e = encode_pool_map(&mk, p.k_cache, kQuant, p.num_pages, p.num_kv_heads, page_size);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) return fail_at(e, "tensor map encode (K)");
   e = encode_pool_map(&mv, p.v_cache, kQuant, p.num_pages, p.num_kv_heads, page_size);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) return fail_at(e, "tensor map encode (V)");
   const dim3 grid(static_cast<unsigned>(p.num_splits), static_cast<unsigned>(p.num_kv_heads),
                   static_cast<unsigned>(bs));
   const bool two_tiles = group > 8;

@@ -112,3 +112,14 @@ def test_instrumented_build_exports_its_header_and_production_does_not():
         assert hasattr(ts, n), n
     prod = ctypes.CDLL(build.LIB_PATH)
     assert not hasattr(prod, "pa_set_timestamp_buffer")
+
+
+def _exported(path):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    return sorted(line.split()[-1] for line in out.splitlines() if line.strip())
+
+
+def test_library_exports_exactly_the_c_abi(lib):
+    assert _exported(build.LIB_PATH) == declared_functions()
