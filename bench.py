@@ -43,6 +43,9 @@ def parse():
                     help="skip the PDL study, e2e and CPU baseline")
     ap.add_argument("--profile", action="store_true",
                     help="eager steps only (warm-up + steps launches of each kernel), for ncu")
+    ap.add_argument("--all-workloads", action="store_true",
+                    help="report table: every named workload, graph with / without PDL and "
+                         "eager (one JSON line per workload; not the benchmark line)")
     return ap.parse_args()
 
 
@@ -476,6 +479,75 @@ def run_gb300(args, spec, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_table(args):
+    """Per-workload latency table (graph replay with and without PDL, eager with PDL),
+    KV bandwidth against the measured peak.  L2: workloads whose inputs fit in the
+    129 MB L2 are also timed rotating over enough copies of the inputs to exceed 2x L2
+    (one CUDA graph per copy, replayed round-robin)."""
+    import torch
+
+    from paged_kv_decode_metadata_gb300 import binding, synthetic
+    from paged_kv_decode_metadata_gb300 import build as pa_build
+    from paged_kv_decode_metadata_gb300.runtime import DeviceStep
+
+    pa_build.build()
+    binding.load()
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    stream = torch.cuda.Stream()
+    l2_bytes = torch.cuda.get_device_properties(0).L2_cache_size
+    for name in synthetic.WORKLOAD_ORDER:
+        wl = synthetic.make(synthetic.WORKLOADS[name])
+        ds = DeviceStep(wl)
+        row = {"workload": name, "num_splits": ds.num_splits}
+        n = max(200, min(args.steps, 2000))
+        for pdl in (False, True):
+            g = capture(torch, lambda: ds.step(use_pdl=pdl), stream)
+            time_graph(torch, g, 50, stream)
+            row["graph_pdl_us" if pdl else "graph_us"] = min(time_graph(torch, g, n, stream)
+                                                            for _ in range(3))
+            del g
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                ds.step(use_pdl=True)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(n):
+                ds.step(use_pdl=True)
+            b.record(stream)
+        b.synchronize()
+        row["eager_pdl_us"] = a.elapsed_time(b) / n * 1e3
+        footprint = ds.step_bytes(wl.ctx)
+        if footprint < 2 * l2_bytes:
+            copies = int(2 * l2_bytes // footprint) + 1
+            steps = [ds] + [DeviceStep(wl) for _ in range(copies - 1)]
+            graphs = [capture(torch, lambda d=d: d.step(use_pdl=True), stream) for d in steps]
+            with torch.cuda.stream(stream):
+                for g in graphs:
+                    g.replay()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                reps = max(1, n // copies)
+                for _ in range(reps):
+                    for g in graphs:
+                        g.replay()
+                b.record(stream)
+            b.synchronize()
+            row["graph_pdl_l2_rotated_us"] = a.elapsed_time(b) / (reps * copies) * 1e3
+            row["l2_rotation_copies"] = copies
+            del graphs, steps
+        best = row.get("graph_pdl_l2_rotated_us", row["graph_pdl_us"])
+        row["kv_bytes"] = ds.kv_bytes(wl.ctx)
+        row["step_bytes"] = footprint
+        row["kv_gbs"] = row["kv_bytes"] / (best * 1e-6) / 1e9
+        row["kv_frac_of_" + peak_kind] = row["kv_gbs"] / hbm_peak
+        if binding.pa_read_error_flags(reset=True):
+            raise RuntimeError("device error flags set")
+        print(json.dumps(row), flush=True)
+        del ds
+        torch.cuda.empty_cache()
+
+
 def run_profile(args, spec):
     """Plain eager decode steps with no timing, sampling or extras: the command that
     ncu captures.  Kernel launch order per step: metadata, split-K producer, reducer."""
@@ -512,6 +584,9 @@ def main():
         return
     if args.profile:
         run_profile(args, spec)
+        return
+    if args.all_workloads:
+        run_table(args)
         return
     if world > 1:
         import torch

@@ -62,16 +62,27 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceParams p) 
   total = warp_sum(total);
   __syncwarp();
 
+  // Batches of 8 independent row loads; an empty split's row is loaded (it lies inside
+  // the scratch buffer) but never used, its contents may be anything.
   const float4* acc = reinterpret_cast<const float4*>(p.acc + row * S * 128) + lane;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < S; ++s) {
-    const float ws = w[s];
-    if (ws != 0.f) {
-      const float4 a = acc[s * 32];
-      o.x = fmaf(ws, a.x, o.x);
-      o.y = fmaf(ws, a.y, o.y);
-      o.z = fmaf(ws, a.z, o.z);
-      o.w = fmaf(ws, a.w, o.w);
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float4 a[8];
+    float ws[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int s = min(s0 + k, S - 1);
+      ws[k] = s0 + k < S ? w[s] : 0.f;
+      a[k] = acc[s * 32];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (ws[k] != 0.f) {
+        o.x = fmaf(ws[k], a[k].x, o.x);
+        o.y = fmaf(ws[k], a[k].y, o.y);
+        o.z = fmaf(ws[k], a[k].z, o.z);
+        o.w = fmaf(ws[k], a[k].w, o.w);
+      }
     }
   }
   trigger_dependents();  // last scratch read done

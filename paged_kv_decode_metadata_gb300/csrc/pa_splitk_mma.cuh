@@ -27,8 +27,10 @@
 //     K = 16 tokens, N = 8 channels.  Q fragments stay in registers for the whole split.
 //   * bf16 KV: K fragments come from ldmatrix, V fragments from ldmatrix.trans.
 //   * int8 KV: 16-byte shared loads of the codes, widened exactly to fp16 in registers
-//     (a byte placed in the mantissa of 1024, minus 1152) and fed to fp16 MMAs (int8
-//     codes are exact in fp16; Q is rounded to fp16, exact for 2^-14 <= |q| <= 65504).
+//     (a byte placed in the mantissa of 1024) and fed to fp16 MMAs (int8 codes are
+//     exact in fp16; Q is rounded to fp16, exact for 2^-14 <= |q| <= 65504).  V codes
+//     are un-biased (minus 1152) before the MMA; K codes enter biased by +1152 and the
+//     resulting 1152 * sum(q) per head is subtracted from the fp32 score.
 //     The contraction order over channels is permuted so that each lane reads
 //     16 contiguous bytes; QK^T does not depend on that order.  The K scale multiplies
 //     the fp32 score, the V scale folds into the softmax weight.
@@ -52,6 +54,8 @@ constexpr int kChunk = 64;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSplitPages = 256;
+// Batches up to this size are dispatched longest request first (see request_for_rank).
+constexpr int kLptMaxBatch = 256;
 
 template <bool kQuant, int STAGES>
 struct Layout {
@@ -63,8 +67,9 @@ struct Layout {
   static constexpr int OFF_FULL = OFF_PAGES + kMaxSplitPages * 4;
   static constexpr int OFF_EMPTY = OFF_FULL + STAGES * 8;
   static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;                    // [4 warps][16 rows][2]
-  static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 2 * 4;    // abort flag, issued
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;                         // + alignment slack
+  static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 2 * 4;    // abort flag, request
+  static constexpr int OFF_LENS = OFF_MISC + 16;                            // [kLptMaxBatch] i32
+  static constexpr int SMEM = OFF_LENS + kLptMaxBatch * 4 + 1024;           // + alignment slack
   static constexpr int RED_BYTES = kConsumerWarps * 16 * 128 * 4;           // output merge buffer
   static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "merge buffer reuses the ring");
 };
@@ -150,6 +155,79 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// B operand of S^T = K Q^T for request b, kv head kvh: b0 = Q[head][k 2tig, 2tig+1],
+// b1 = Q[head][k 2tig+8, +9] of k-step j, head = 8 * nt + gid (zero for heads >= G).
+// int8 path (kF16): fp16 Q in the permuted contraction order (k-step j, lane tig ->
+// channels 32*tig + 4*j + {0..3}), plus kbias: the K codes enter the MMA biased by
+// +1152 (the widening skips the subtract), so each score carries 1152 * sum_d q[h][d];
+// kbias[nt][e] (head 8nt + 2tig + e) is that offset from the same fp16 Q values.
+template <bool kF16, int kNT>
+__device__ __forceinline__ void load_q_fragments(const SplitKParams& prm, int b, int kvh, int G,
+                                                 int gid, int tig, uint32_t (&qb)[kNT][8][2],
+                                                 float (&kbias)[kNT][2]) {
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+    const int head = 8 * nt + gid;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t lo = 0, hi = 0;
+      if (head < G) {
+        const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(prm.q) +
+                                  (static_cast<int64_t>(b) * prm.num_q_heads + kvh * G + head) * 128;
+        if constexpr (kF16) {
+          const int d = 32 * tig + 4 * j;
+          lo = pack_f16(__bfloat162float(qr[d]), __bfloat162float(qr[d + 1]));
+          hi = pack_f16(__bfloat162float(qr[d + 2]), __bfloat162float(qr[d + 3]));
+        } else {
+          const int d = 16 * j + 2 * tig;
+          lo = *reinterpret_cast<const uint32_t*>(qr + d);
+          hi = *reinterpret_cast<const uint32_t*>(qr + d + 8);
+        }
+      }
+      qb[nt][j][0] = lo;
+      qb[nt][j][1] = hi;
+    }
+    kbias[nt][0] = kbias[nt][1] = 0.f;
+    if constexpr (kF16) {
+      float part = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qb[nt][j][0]));
+        const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&qb[nt][j][1]));
+        part += (a.x + a.y) + (c.x + c.y);
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);  // sum over the head's 128 channels
+      kbias[nt][0] = 1152.f * __shfl_sync(0xffffffffu, part, (2 * tig) * 4);
+      kbias[nt][1] = 1152.f * __shfl_sync(0xffffffffu, part, (2 * tig + 1) * 4);
+    }
+  }
+}
+
+// Request handled by the blocks at position `rank` of the grid's request axis: the
+// requests in order of decreasing cache length (ties by index).  Blocks are dispatched
+// in grid order, so the longest requests start first and the short ones fill the tail
+// of a ragged batch.  Every (request, kv head, split) computes the same partials
+// whichever block runs it.  Batches larger than kLptMaxBatch keep the grid order.
+// All threads of the block call this (it synchronises the block).
+__device__ __forceinline__ int request_for_rank(const int32_t* cache_seqlens, int bs, int rank,
+                                                int32_t* lens_s, int* slot) {
+  if (bs <= 1 || bs > kLptMaxBatch) return rank;
+  for (int i = threadIdx.x; i < bs; i += blockDim.x) lens_s[i] = cache_seqlens[i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < bs; i += blockDim.x) {
+    const int li = lens_s[i];
+    int r = 0;
+    for (int j = 0; j < bs; ++j) {
+      const int lj = lens_s[j];
+      r += (lj > li) || (lj == li && j < i);
+    }
+    if (r == rank) *slot = i;
+  }
+  __syncthreads();
+  return *slot;
+}
+
 template <bool kQuant, int P, int STAGES, int MINB, int kNT>
 __global__ void __launch_bounds__(kThreads, MINB)
     splitk_mma_kernel(const __grid_constant__ CUtensorMap map_k,
@@ -161,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t smem_base = smem_addr(smem);
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, kvh = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int G = prm.num_q_heads / prm.num_kv_heads;
@@ -176,33 +254,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC);
 
   // ---- prologue independent of the metadata stage: Q^T fragments in registers ------
-  // B operand of S^T = K Q^T: b0 = Q[head][k 2tig, 2tig+1], b1 = Q[head][k 2tig+8, +9]
-  // of k-step j, head = 8 * nt + gid.
+  // (for the request this block would take in grid order; see request_for_rank below)
+  int b = blockIdx.z;
   uint32_t qb[kNT][8][2];
-#pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) {
-    const int head = 8 * nt + gid;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t lo = 0, hi = 0;
-      if (is_consumer && head < G) {
-        const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(prm.q) +
-                                  (static_cast<int64_t>(b) * prm.num_q_heads + kvh * G + head) * 128;
-        if constexpr (kF16) {
-          // contraction order: k-step j, lane tig -> channels 32*tig + 4*j + {0..3}
-          const int d = 32 * tig + 4 * j;
-          lo = pack_f16(__bfloat162float(qr[d]), __bfloat162float(qr[d + 1]));
-          hi = pack_f16(__bfloat162float(qr[d + 2]), __bfloat162float(qr[d + 3]));
-        } else {
-          const int d = 16 * j + 2 * tig;
-          lo = *reinterpret_cast<const uint32_t*>(qr + d);
-          hi = *reinterpret_cast<const uint32_t*>(qr + d + 8);
-        }
-      }
-      qb[nt][j][0] = lo;
-      qb[nt][j][1] = hi;
-    }
-  }
+  float kbias[kNT][2];
+  if (is_consumer) load_q_fragments<kF16, kNT>(prm, b, kvh, G, gid, tig, qb, kbias);
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -215,6 +271,16 @@ __global__ void __launch_bounds__(kThreads, MINB)
   // ---- everything below reads what the metadata stage wrote -------------------------
   grid_dependency_wait();
   PA_TS_FIRST(prm.ts, 1, kTsReady);
+
+  {
+    const int ranked = request_for_rank(prm.cache_seqlens, gridDim.z, blockIdx.z,
+                                        reinterpret_cast<int32_t*>(smem + L::OFF_LENS),
+                                        reinterpret_cast<int*>(smem + L::OFF_MISC + 8));
+    if (ranked != b) {
+      b = ranked;
+      if (is_consumer) load_q_fragments<kF16, kNT>(prm, b, kvh, G, gid, tig, qb, kbias);
+    }
+  }
 
   int n = prm.cache_seqlens[b];
   const int cap = prm.max_seq_pages * P;
@@ -415,10 +481,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int j = 0; j < 8; ++j) {
           const uint32_t x0 = w0[j] ^ 0x80808080u, x1 = w1[j] ^ 0x80808080u;
           uint32_t a[4];
-          a[0] = biased_bytes_to_f16x2(x0, 0x4140);  // token gid,     channels +0, +1
-          a[1] = biased_bytes_to_f16x2(x1, 0x4140);  // token gid + 8
-          a[2] = biased_bytes_to_f16x2(x0, 0x4342);  // token gid,     channels +2, +3
-          a[3] = biased_bytes_to_f16x2(x1, 0x4342);  // token gid + 8
+          // 1024 + (code + 128) = code + 1152, exact in fp16; the +1152 is removed
+          // from the score through kbias
+          a[0] = __byte_perm(x0, 0x64646464u, 0x4140);  // token gid,     channels +0, +1
+          a[1] = __byte_perm(x1, 0x64646464u, 0x4140);  // token gid + 8
+          a[2] = __byte_perm(x0, 0x64646464u, 0x4342);  // token gid,     channels +2, +3
+          a[3] = __byte_perm(x1, 0x64646464u, 0x4342);  // token gid + 8
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt) mma16816<true>(acc[j & 1][nt], a, qb[nt][j][0], qb[nt][j][1]);
         }
@@ -441,7 +509,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
         float x[4];  // (token a, head e0), (a, e1), (b, e0), (b, e1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          float v = (acc[0][nt][i] + acc[1][nt][i]) * q_scale;
+          float v = (acc[0][nt][i] + acc[1][nt][i]);
+          if constexpr (kQuant) v -= kbias[nt][i & 1];
+          v *= q_scale;
           if constexpr (kQuant) v *= (i < 2 ? ks_a : ks_b);
           x[i] = (i < 2 ? tok_a : tok_b) < valid ? v : -CUDART_INF_F;
         }
