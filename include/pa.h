@@ -117,9 +117,11 @@ PA_API pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_
                             int32_t page_size, void* stream, int32_t use_pdl);
 
 /*
- * pa_build_metadata_full -- pa_build_metadata plus the optional outputs of the same
- * module: cu_seqlens_q in the three modes above (qlens [bs] int64 device pointer for
- * PA_Q_MODE_CUMSUM, cu_seqlens_q [bs+1] int32 for modes 1 and 2), and the
+ * pa_build_metadata_full -- pa_build_metadata plus the other inputs and optional outputs
+ * of the same module.  The [bs] index inputs (req_pool_indices, seq_lens, qlens; "int"
+ * in the module's kernel signature) are int64 or int32 per index_bits (64 or 32).
+ * cu_seqlens_q in the three modes above (qlens [bs] for PA_Q_MODE_CUMSUM,
+ * cu_seqlens_q [bs+1] int32 for modes 1 and 2), and the
  * sliding-window translation of the step's output slots:
  *   for idx < swa_out_len:  idx < num_out_tokens -> loc = out_cache_loc[idx];
  *                                                   loc < 0 ? -1 : full_to_swa_mapping[loc]
@@ -128,10 +130,10 @@ PA_API pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_
  * swa_out_cache_loc [swa_out_len] int64 (out) or NULL; it needs the mapping.
  */
 PA_API pa_status pa_build_metadata_full(
-    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
-    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const void* req_pool_indices, const void* seq_lens, int32_t index_bits,
+    const int32_t* req_to_token, int64_t req_to_token_rows, int64_t req_to_token_stride,
     const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
-    const int64_t* out_cache_loc, int64_t out_cache_loc_len, const int64_t* qlens,
+    const int64_t* out_cache_loc, int64_t out_cache_loc_len, const void* qlens,
     int32_t* cache_seqlens, int32_t* cu_seqlens_k, int32_t* cu_seqlens_q,
     int32_t* page_table, int64_t page_table_stride, int32_t* swa_page_table,
     int64_t swa_page_table_stride, int64_t* swa_out_cache_loc, int64_t swa_out_len,

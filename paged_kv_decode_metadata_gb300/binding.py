@@ -85,9 +85,9 @@ def _declare(lib):
                              ctypes.c_size_t)
     lib.pa_build_metadata.argtypes = [vp, vp, vp, i64, i64, vp, i64, vp, vp, vp, i64, vp, i64,
                                       i32, i32, i32, i32, vp, i32]
-    lib.pa_build_metadata_full.argtypes = [vp, vp, vp, i64, i64, vp, i64, vp, i64, vp, vp, vp,
-                                           vp, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32,
-                                           i32, i32, vp, i32]
+    lib.pa_build_metadata_full.argtypes = [vp, vp, i32, vp, i64, i64, vp, i64, vp, i64, vp, vp,
+                                           vp, vp, vp, i64, vp, i64, vp, i64, i32, i32, i32,
+                                           i32, i32, i32, vp, i32]
     lib.pa_decode_splitk.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, i32, i32, i32, i32,
                                      i32, i64, i32, i32, f32, vp, vp, vp, vp, i32]
     lib.pa_reduce.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32]
@@ -183,16 +183,19 @@ def pa_build_metadata_full(req_pool_indices, seq_lens, req_to_token, cache_seqle
     bs = req_pool_indices.shape[0]
     pt_stride = _row_stride(page_table, "page_table")
     swa_stride = _row_stride(swa_page_table, "swa_page_table") if swa_page_table is not None else 0
+    idx_dtype = req_pool_indices.dtype
+    if idx_dtype not in (torch.int64, torch.int32):
+        raise ValueError("req_pool_indices must be int64 or int32")
     st = lib.pa_build_metadata_full(
-        _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
-        _ptr(seq_lens, torch.int64, "seq_lens"),
+        _ptr(req_pool_indices, idx_dtype, "req_pool_indices"),
+        _ptr(seq_lens, idx_dtype, "seq_lens"), 64 if idx_dtype == torch.int64 else 32,
         _ptr2d(req_to_token, torch.int32, "req_to_token"),
         req_to_token.shape[0], req_to_token.stride(0),
         _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
         full_to_swa_mapping.numel() if full_to_swa_mapping is not None else 0,
         _ptr(out_cache_loc, torch.int64, "out_cache_loc"),
         out_cache_loc.numel() if out_cache_loc is not None else 0,
-        _ptr(qlens, torch.int64, "qlens"),
+        _ptr(qlens, idx_dtype, "qlens"),
         _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
         _ptr(cu_seqlens_k, torch.int32, "cu_seqlens_k"),
         _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q"),

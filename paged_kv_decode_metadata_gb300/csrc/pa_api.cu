@@ -69,7 +69,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-pa_status check_metadata(const int64_t* req_pool_indices, const int64_t* seq_lens,
+pa_status check_metadata(const void* req_pool_indices, const void* seq_lens,
                          const int32_t* req_to_token, int64_t req_to_token_rows,
                          int64_t req_to_token_stride, const int64_t* mapping,
                          int64_t mapping_len, int32_t* cache_seqlens, int32_t* cu_seqlens_k,
@@ -136,15 +136,16 @@ pa_status launch_metadata_checked(const pa::MetadataParams& p, cudaStream_t stre
 extern "C" {
 
 pa_status pa_build_metadata_full(
-    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
-    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const void* req_pool_indices, const void* seq_lens, int32_t index_bits,
+    const int32_t* req_to_token, int64_t req_to_token_rows, int64_t req_to_token_stride,
     const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
-    const int64_t* out_cache_loc, int64_t out_cache_loc_len, const int64_t* qlens,
+    const int64_t* out_cache_loc, int64_t out_cache_loc_len, const void* qlens,
     int32_t* cache_seqlens, int32_t* cu_seqlens_k, int32_t* cu_seqlens_q,
     int32_t* page_table, int64_t page_table_stride, int32_t* swa_page_table,
     int64_t swa_page_table_stride, int64_t* swa_out_cache_loc, int64_t swa_out_len,
     int32_t bs, int32_t seqlen_offset, int32_t max_seq_pages, int32_t page_size,
     int32_t q_mode, int32_t q_stride, void* stream, int32_t use_pdl) {
+  if (index_bits != 32 && index_bits != 64) return PA_ERR_INVALID;
   pa_status st = check_metadata(req_pool_indices, seq_lens, req_to_token, req_to_token_rows,
                                 req_to_token_stride, full_to_swa_mapping,
                                 full_to_swa_mapping_len, cache_seqlens, cu_seqlens_k,
@@ -188,6 +189,7 @@ pa_status pa_build_metadata_full(
   p.page_size = page_size;
   p.q_mode = q_mode;
   p.q_stride = q_stride;
+  p.idx64 = index_bits == 64;
   p.ts = g_ts.load();
   cudaError_t e = error_word(&p.err);
   if (e != cudaSuccess) return from_cuda(e, "error word lookup");
@@ -205,7 +207,7 @@ pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_t* seq_
                             int32_t seqlen_offset, int32_t max_seq_pages,
                             int32_t page_size, void* stream, int32_t use_pdl) {
   return pa_build_metadata_full(
-      req_pool_indices, seq_lens, req_to_token, req_to_token_rows, req_to_token_stride,
+      req_pool_indices, seq_lens, 64, req_to_token, req_to_token_rows, req_to_token_stride,
       full_to_swa_mapping, full_to_swa_mapping_len, nullptr, 0, nullptr, cache_seqlens,
       cu_seqlens_k, nullptr, page_table, page_table_stride, swa_page_table,
       swa_page_table_stride, nullptr, 0, bs, seqlen_offset, max_seq_pages, page_size,

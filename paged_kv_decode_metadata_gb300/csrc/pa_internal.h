@@ -7,8 +7,8 @@
 namespace pa {
 
 struct MetadataParams {
-  const int64_t* req_pool_indices;
-  const int64_t* seq_lens;
+  const void* req_pool_indices;  // int64 or int32 (idx64)
+  const void* seq_lens;          // int64 or int32 (idx64)
   const int32_t* req_to_token;
   int64_t req_to_token_rows;
   int64_t req_to_token_stride;
@@ -16,7 +16,7 @@ struct MetadataParams {
   int64_t mapping_len;
   const int64_t* out_cache_loc;
   int64_t num_out_tokens;  // valid prefix of out_cache_loc (already min'ed)
-  const int64_t* qlens;
+  const void* qlens;  // int64 or int32 (idx64)
   int32_t* cache_seqlens;
   int32_t* cu_seqlens_k;
   int32_t* cu_seqlens_q;
@@ -32,6 +32,7 @@ struct MetadataParams {
   int32_t page_size;
   int32_t q_mode;
   int32_t q_stride;
+  bool idx64;  // index inputs are int64 (else int32)
   unsigned int* err;
   unsigned long long* ts;  // stage timestamps (instrumented builds only), else nullptr
 };

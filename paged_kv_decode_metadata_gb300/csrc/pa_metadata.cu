@@ -23,6 +23,12 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Index inputs ([bs] "int" in the source module) may be int64 or int32.
+__device__ __forceinline__ int64_t load_index(const void* p, int64_t i, bool is64) {
+  return is64 ? static_cast<const int64_t*>(p)[i]
+              : static_cast<int64_t>(static_cast<const int32_t*>(p)[i]);
+}
+
 // Block-wide inclusive scan of one uint32 per thread (wrapping adds).  Returns the
 // thread's inclusive prefix; *total receives the block total.
 __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_sums,
@@ -63,14 +69,14 @@ __global__ void __launch_bounds__(kThreads) metadata_kernel(const MetadataParams
   if (blk < p.bs) {
     // ---- one request row -------------------------------------------------------
     const int i = blk;
-    int64_t row = p.req_pool_indices[i];
+    int64_t row = load_index(p.req_pool_indices, i, p.idx64);
     const bool row_ok = row >= 0 && row < p.req_to_token_rows;
     if (!row_ok) {
       if (tid == 0) record_error(p.err, kErrPoolRowOutOfRange);
       row = 0;
     }
     if (tid == 0) {
-      const uint64_t sum = static_cast<uint64_t>(p.seq_lens[i]) +
+      const uint64_t sum = static_cast<uint64_t>(load_index(p.seq_lens, i, p.idx64)) +
                            static_cast<uint64_t>(static_cast<int64_t>(p.seqlen_offset));
       p.cache_seqlens[i] = static_cast<int32_t>(static_cast<uint32_t>(sum));
     }
@@ -104,7 +110,7 @@ __global__ void __launch_bounds__(kThreads) metadata_kernel(const MetadataParams
     uint32_t carry = 0;
     for (int base = 0; base < p.bs; base += kThreads) {
       const int j = base + tid;
-      const uint32_t v = j < p.bs ? static_cast<uint32_t>(p.seq_lens[j]) +
+      const uint32_t v = j < p.bs ? static_cast<uint32_t>(load_index(p.seq_lens, j, p.idx64)) +
                                         static_cast<uint32_t>(p.seqlen_offset)
                                   : 0u;
       uint32_t total;
@@ -117,7 +123,7 @@ __global__ void __launch_bounds__(kThreads) metadata_kernel(const MetadataParams
       carry = 0;
       for (int base = 0; base < p.bs; base += kThreads) {
         const int j = base + tid;
-        const uint32_t v = j < p.bs ? static_cast<uint32_t>(p.qlens[j]) : 0u;
+        const uint32_t v = j < p.bs ? static_cast<uint32_t>(load_index(p.qlens, j, p.idx64)) : 0u;
         uint32_t total;
         const uint32_t incl = block_inclusive_scan(v, warp_sums, &total);
         if (j < p.bs) p.cu_seqlens_q[j + 1] = static_cast<int32_t>(incl + carry);

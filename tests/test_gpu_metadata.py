@@ -120,8 +120,10 @@ def test_metadata_hand_example_and_full_surface():
     assert cq.tolist() == qc["strided"]
 
 
-def test_metadata_full_surface_against_oracle():
-    """Large batch (several scan tiles), random qlens, long swa_out_cache_loc."""
+@pytest.mark.parametrize("idx", [torch.int64, torch.int32])
+def test_metadata_full_surface_against_oracle(idx):
+    """Large batch (several scan tiles), random qlens, long swa_out_cache_loc; index
+    inputs as int64 and as int32 (the module's kernel takes either)."""
     g = torch.Generator().manual_seed(77)
     spec = synthetic.Spec("scan", bs=700, num_q_heads=8, num_kv_heads=8, num_pages=12000,
                           ragged=(0, 900), swa_window=200, seqlen_offset=1, seed=78)
@@ -135,10 +137,11 @@ def test_metadata_full_surface_against_oracle():
     cl, cu, cq = torch.empty(spec.bs, **i32), torch.empty(spec.bs + 1, **i32), torch.empty(spec.bs + 1, **i32)
     pt, swa = torch.empty((spec.bs, msp), **i32), torch.empty((spec.bs, msp), **i32)
     swa_out = torch.full((1700,), 5, dtype=torch.int64, device=dev)
-    B.pa_build_metadata_full(wl.req_pool_indices.to(dev), wl.seq_lens.to(dev), wl.req_to_token.to(dev),
-                             cl, cu, pt, seqlen_offset=1, max_seq_pages=msp, page_size=64,
-                             full_to_swa_mapping=full.to(dev), swa_page_table=swa, cu_seqlens_q=cq,
-                             qlens=qlens.to(dev), q_mode=B.PA_Q_MODE_CUMSUM, out_cache_loc=loc.to(dev),
+    B.pa_build_metadata_full(wl.req_pool_indices.to(dev, idx), wl.seq_lens.to(dev, idx),
+                             wl.req_to_token.to(dev), cl, cu, pt, seqlen_offset=1,
+                             max_seq_pages=msp, page_size=64, full_to_swa_mapping=full.to(dev),
+                             swa_page_table=swa, cu_seqlens_q=cq, qlens=qlens.to(dev, idx),
+                             q_mode=B.PA_Q_MODE_CUMSUM, out_cache_loc=loc.to(dev),
                              swa_out_cache_loc=swa_out)
     torch.cuda.synchronize()
     want = oracle_metadata(wl)
