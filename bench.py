@@ -246,19 +246,25 @@ def capture(torch, fn, stream):
     return graph
 
 
-def pdl_study(torch, synthetic, DeviceStep, stream, replays=3000):
-    """Graph-replay and eager latency with and without PDL at batch 1."""
+def pdl_study(torch, synthetic, DeviceStep, stream, replays=300, steps_per_graph=16):
+    """Batch-1 decode-step latency with and without PDL.  One CUDA graph holds
+    `steps_per_graph` consecutive steps (48 kernels), so graph-launch overhead on the
+    host is amortised and the time per step is the GPU's, including the step-to-step
+    hand-off; eager: back-to-back C-ABI calls."""
     out = {}
     for name in ("bs1_ctx1k", "bs1_ctx8k"):
         wl = synthetic.make(synthetic.WORKLOADS[name])
         ds = DeviceStep(wl)
         row = {}
         for pdl in (False, True):
-            g = capture(torch, lambda: ds.step(use_pdl=pdl), stream)
+            def steps(pdl=pdl):
+                for _ in range(steps_per_graph):
+                    ds.step(use_pdl=pdl)
+            g = capture(torch, steps, stream)
             for _ in range(3):
-                time_graph(torch, g, 200, stream)
+                time_graph(torch, g, 20, stream)
             row["graph_pdl_us" if pdl else "graph_us"] = min(
-                time_graph(torch, g, replays, stream) for _ in range(3))
+                time_graph(torch, g, replays, stream) for _ in range(3)) / steps_per_graph
             del g
             with torch.cuda.stream(stream):
                 for _ in range(50):
@@ -271,6 +277,7 @@ def pdl_study(torch, synthetic, DeviceStep, stream, replays=3000):
             end.synchronize()
             row["eager_pdl_us" if pdl else "eager_us"] = start.elapsed_time(end) / 500 * 1e3
         row["num_splits"] = ds.num_splits
+        row["steps_per_graph"] = steps_per_graph
         out[name] = row
         del ds
     return out

@@ -74,11 +74,14 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_swa_out_cache_loc.argtypes = [vp, i64, vp, vp, i64]
     lib.oracle_paged_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, i32, i32,
                                            i32, i32, i32, f64, vp, vp]
+    lib.oracle_paged_attention_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, vp, i32,
+                                                 i32, i32, i32, i32, f64, vp, vp]
     lib.oracle_splitk_partials.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, i32, i32,
                                            i32, i32, i32, i32, i32, f64, vp, vp, vp]
     lib.oracle_combine_splits.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
     for name in ("oracle_build_metadata", "oracle_cu_seqlens_q", "oracle_swa_out_cache_loc",
-                 "oracle_paged_attention", "oracle_splitk_partials", "oracle_combine_splits"):
+                 "oracle_paged_attention", "oracle_paged_attention_multi",
+                 "oracle_splitk_partials", "oracle_combine_splits"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -175,6 +178,28 @@ def paged_attention(q_bits, k_cache, v_cache, page_table, cache_seqlens, sm_scal
     lib.oracle_paged_attention(_p(q), _p(k), _p(v), _p(ks), _p(vs), kv_dtype, _p(pt),
                                pt.shape[1], _p(cl), bs, hq, hkv, d, page_size,
                                float(sm_scale), _p(out), _p(lse))
+    return out, lse
+
+
+def paged_attention_multi(q_bits, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
+                          sm_scale, k_scale=None, v_scale=None, lib=None):
+    """Several query tokens per request, causal within the request's newest tokens.
+
+    ``q_bits`` [total_q, Hq, d] uint16; ``cu_seqlens_q`` [bs + 1] int32.  Returns
+    (out [total_q, Hq, d], lse [total_q, Hq]) in float64.
+    """
+    lib = lib or load()
+    q, k, v, ks, vs, kv_dtype = _attention_args(q_bits, k_cache, v_cache, k_scale, v_scale)
+    pt = _c(page_table, np.int32)
+    cl = _c(cache_seqlens, np.int32)
+    cq = _c(cu_seqlens_q, np.int32)
+    total_q, hq, d = q.shape
+    _, hkv, page_size, _ = k.shape
+    out = np.zeros((total_q, hq, d), np.float64)
+    lse = np.zeros((total_q, hq), np.float64)
+    lib.oracle_paged_attention_multi(_p(q), _p(k), _p(v), _p(ks), _p(vs), kv_dtype, _p(pt),
+                                     pt.shape[1], _p(cl), _p(cq), cl.shape[0], hq, hkv, d,
+                                     page_size, float(sm_scale), _p(out), _p(lse))
     return out, lse
 
 

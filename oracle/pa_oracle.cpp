@@ -18,6 +18,9 @@
 //     paged attention and V4 prefill", section Changes / Split-K paged attention)
 //     but do not print the attention arithmetic, so this is the textbook
 //     definition of scaled dot-product attention with grouped KV heads.
+//   * oracle_paged_attention_multi - the same attention for several query tokens per
+//     request (rows given by cu_seqlens_q, the module's query-length output), causal
+//     within the request's newest tokens.
 //   * oracle_splitk_partials  - the per-split partial results (running max m,
 //     sum of exponentials l, unnormalised accumulator acc) that the split-K
 //     producer writes to scratch, for a given split of the context.
@@ -206,6 +209,66 @@ int oracle_paged_attention(const uint16_t* q, const void* k_cache, const void* v
         }
       }
       lse[static_cast<int64_t>(b) * num_q_heads + h] = x_max + std::log(denom);
+    }
+  }
+  return 0;
+}
+
+// Several query tokens per request (speculative verify / extend steps).  Query rows of
+// request b are q[cu_seqlens_q[b] .. cu_seqlens_q[b+1]) ([total_q][num_q_heads][head_dim]);
+// they are the last q_len = cu_seqlens_q[b+1] - cu_seqlens_q[b] tokens of the request's
+// cache, so query i attends causally to token positions j < n - q_len + i + 1 with
+// n = cache_seqlens[b] (an empty range gives out = 0 and lse = -inf).  Everything else
+// is oracle_paged_attention.  out [total_q][num_q_heads][head_dim], lse [total_q][num_q_heads].
+int oracle_paged_attention_multi(const uint16_t* q, const void* k_cache, const void* v_cache,
+                                 const float* k_scale, const float* v_scale, int32_t kv_dtype,
+                                 const int32_t* page_table, int64_t page_table_stride,
+                                 const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
+                                 int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t page_size, double sm_scale,
+                                 double* out, double* lse) {
+  const int32_t group = num_q_heads / num_kv_heads;
+  for (int32_t b = 0; b < bs; ++b) {
+    const int32_t q_begin = cu_seqlens_q[b];
+    const int32_t q_len = cu_seqlens_q[b + 1] - q_begin;
+    for (int32_t i = 0; i < q_len; ++i) {
+      const int64_t row = q_begin + i;
+      const int64_t limit = static_cast<int64_t>(cache_seqlens[b]) - q_len + i + 1;
+      const int32_t n = limit > 0 ? static_cast<int32_t>(limit) : 0;
+      for (int32_t h = 0; h < num_q_heads; ++h) {
+        const int32_t kv_head = h / group;
+        const uint16_t* qrow = q + (row * num_q_heads + h) * head_dim;
+        double* orow = out + (row * num_q_heads + h) * head_dim;
+        for (int32_t c = 0; c < head_dim; ++c) orow[c] = 0.0;
+        if (n == 0) {
+          lse[row * num_q_heads + h] = -std::numeric_limits<double>::infinity();
+          continue;
+        }
+        std::vector<double> x(n);
+        double x_max = -std::numeric_limits<double>::infinity();
+        for (int32_t j = 0; j < n; ++j) {
+          const int64_t page = page_table[b * page_table_stride + j / page_size];
+          double dot = 0.0;
+          for (int32_t c = 0; c < head_dim; ++c) {
+            dot += bf16_bits_to_double(qrow[c]) *
+                   kv_element(k_cache, k_scale, kv_dtype, page, kv_head, j % page_size, c,
+                              num_kv_heads, page_size, head_dim);
+          }
+          x[j] = sm_scale * dot;
+          if (x[j] > x_max) x_max = x[j];
+        }
+        double denom = 0.0;
+        for (int32_t j = 0; j < n; ++j) denom += std::exp(x[j] - x_max);
+        for (int32_t j = 0; j < n; ++j) {
+          const int64_t page = page_table[b * page_table_stride + j / page_size];
+          const double w = std::exp(x[j] - x_max) / denom;
+          for (int32_t c = 0; c < head_dim; ++c) {
+            orow[c] += w * kv_element(v_cache, v_scale, kv_dtype, page, kv_head, j % page_size, c,
+                                      num_kv_heads, page_size, head_dim);
+          }
+        }
+        lse[row * num_q_heads + h] = x_max + std::log(denom);
+      }
     }
   }
   return 0;

@@ -54,8 +54,12 @@ constexpr int kChunk = 64;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSplitPages = 256;
-// Batches up to this size are dispatched longest request first (see request_for_rank).
-constexpr int kLptMaxBatch = 256;
+// Batches up to this size are dispatched longest request first (see request_for_rank);
+// 0 keeps the grid order for every batch.
+#ifndef PA_LPT_MAX_BATCH
+#define PA_LPT_MAX_BATCH 256
+#endif
+constexpr int kLptMaxBatch = PA_LPT_MAX_BATCH;
 
 template <bool kQuant, int STAGES>
 struct Layout {
@@ -69,7 +73,7 @@ struct Layout {
   static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;                    // [4 warps][16 rows][2]
   static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 2 * 4;    // abort flag, request
   static constexpr int OFF_LENS = OFF_MISC + 16;                            // [kLptMaxBatch] i32
-  static constexpr int SMEM = OFF_LENS + kLptMaxBatch * 4 + 1024;           // + alignment slack
+  static constexpr int SMEM = OFF_LENS + (kLptMaxBatch > 0 ? kLptMaxBatch : 1) * 4 + 1024;
   static constexpr int RED_BYTES = kConsumerWarps * 16 * 128 * 4;           // output merge buffer
   static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "merge buffer reuses the ring");
 };

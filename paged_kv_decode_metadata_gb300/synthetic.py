@@ -182,6 +182,19 @@ def _swa_mapping(spec: Spec, ctx, pages, g):
     return mapping, swa_pages, window_start
 
 
+def draw_query_lengths(bs: int, max_q_len: int, seed: int) -> torch.Tensor:
+    """Query tokens per request for multi-token (speculative verify / extend) steps:
+    uniform in 1..max_q_len, int64 [bs]."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(1, max_q_len + 1, (bs,), generator=g, dtype=torch.int64)
+
+
+def draw_queries(total_q: int, num_q_heads: int, head_dim: int, seed: int) -> torch.Tensor:
+    """Query rows ~ N(0, 1) in bf16, [total_q, num_q_heads, head_dim]."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((total_q, num_q_heads, head_dim), generator=g).to(torch.bfloat16)
+
+
 def small_spec(seed: int, kv_dtype: str = "bf16", bs_max: int = 5, ctx_max: int = 300,
                group: Optional[int] = None, num_splits: Optional[int] = None,
                page_size: int = 64) -> Spec:
