@@ -54,12 +54,6 @@ constexpr int kChunk = 64;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSplitPages = 256;
-// Batches up to this size are dispatched longest request first (see request_for_rank);
-// 0 keeps the grid order for every batch.
-#ifndef PA_LPT_MAX_BATCH
-#define PA_LPT_MAX_BATCH 256
-#endif
-constexpr int kLptMaxBatch = PA_LPT_MAX_BATCH;
 
 template <bool kQuant, int STAGES>
 struct Layout {
@@ -71,9 +65,8 @@ struct Layout {
   static constexpr int OFF_FULL = OFF_PAGES + kMaxSplitPages * 4;
   static constexpr int OFF_EMPTY = OFF_FULL + STAGES * 8;
   static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;                    // [4 warps][16 rows][2]
-  static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 2 * 4;    // abort flag, request
-  static constexpr int OFF_LENS = OFF_MISC + 16;                            // [kLptMaxBatch] i32
-  static constexpr int SMEM = OFF_LENS + (kLptMaxBatch > 0 ? kLptMaxBatch : 1) * 4 + 1024;
+  static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 2 * 4;    // abort flag
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;                         // + alignment slack
   static constexpr int RED_BYTES = kConsumerWarps * 16 * 128 * 4;           // output merge buffer
   static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "merge buffer reuses the ring");
 };
@@ -208,30 +201,6 @@ __device__ __forceinline__ void load_q_fragments(const SplitKParams& prm, int b,
   }
 }
 
-// Request handled by the blocks at position `rank` of the grid's request axis: the
-// requests in order of decreasing cache length (ties by index).  Blocks are dispatched
-// in grid order, so the longest requests start first and the short ones fill the tail
-// of a ragged batch.  Every (request, kv head, split) computes the same partials
-// whichever block runs it.  Batches larger than kLptMaxBatch keep the grid order.
-// All threads of the block call this (it synchronises the block).
-__device__ __forceinline__ int request_for_rank(const int32_t* cache_seqlens, int bs, int rank,
-                                                int32_t* lens_s, int* slot) {
-  if (bs <= 1 || bs > kLptMaxBatch) return rank;
-  for (int i = threadIdx.x; i < bs; i += blockDim.x) lens_s[i] = cache_seqlens[i];
-  __syncthreads();
-  for (int i = threadIdx.x; i < bs; i += blockDim.x) {
-    const int li = lens_s[i];
-    int r = 0;
-    for (int j = 0; j < bs; ++j) {
-      const int lj = lens_s[j];
-      r += (lj > li) || (lj == li && j < i);
-    }
-    if (r == rank) *slot = i;
-  }
-  __syncthreads();
-  return *slot;
-}
-
 template <bool kQuant, int P, int STAGES, int MINB, int kNT>
 __global__ void __launch_bounds__(kThreads, MINB)
     splitk_mma_kernel(const __grid_constant__ CUtensorMap map_k,
@@ -258,8 +227,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC);
 
   // ---- prologue independent of the metadata stage: Q^T fragments in registers ------
-  // (for the request this block would take in grid order; see request_for_rank below)
-  int b = blockIdx.z;
+  const int b = blockIdx.z;
   uint32_t qb[kNT][8][2];
   float kbias[kNT][2];
   if (is_consumer) load_q_fragments<kF16, kNT>(prm, b, kvh, G, gid, tig, qb, kbias);
@@ -276,15 +244,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
   grid_dependency_wait();
   PA_TS_FIRST(prm.ts, 1, kTsReady);
 
-  {
-    const int ranked = request_for_rank(prm.cache_seqlens, gridDim.z, blockIdx.z,
-                                        reinterpret_cast<int32_t*>(smem + L::OFF_LENS),
-                                        reinterpret_cast<int*>(smem + L::OFF_MISC + 8));
-    if (ranked != b) {
-      b = ranked;
-      if (is_consumer) load_q_fragments<kF16, kNT>(prm, b, kvh, G, gid, tig, qb, kbias);
-    }
-  }
 
   int n = prm.cache_seqlens[b];
   const int cap = prm.max_seq_pages * P;
