@@ -184,6 +184,30 @@ PA_API pa_status pa_decode_splitk(const void* q, const void* k_cache, const void
                            float* scratch_acc, void* stream, int32_t use_pdl);
 
 /*
+ * pa_decode_splitk_multi -- the producer for several query tokens per request
+ * (speculative target-verify / draft-extend steps, whose query lengths the metadata
+ * module's cu_seqlens_q describes).  Query rows of request b are
+ * q[cu_seqlens_q[b] .. cu_seqlens_q[b+1]) ([total_q, num_q_heads, head_dim] bf16), at most
+ * max_q_len per request; they are the request's newest tokens, already in its cache,
+ * so query i (0-based) attends causally to token positions j < n - q_len + i + 1,
+ * n = cache_seqlens[b].  Splits, layouts and partial semantics are those of
+ * pa_decode_splitk with one scratch row per query row: scratch_m/l
+ * [total_q, num_q_heads, num_splits], scratch_acc [total_q, num_q_heads, num_splits,
+ * head_dim]; pa_reduce with bs = total_q combines them.  cu_seqlens_q [bs+1] int32 is
+ * read after the wait on the previous grid (it may be the metadata stage's output).
+ * Tensor-core producer only: PA_ERR_UNSUPPORTED when (num_q_heads/num_kv_heads) *
+ * max_q_len > 16 or the CUDA-core producer is selected.  A query whose causal range is
+ * empty gets m = -inf in every split (out = 0, lse = -inf after pa_reduce).
+ */
+PA_API pa_status pa_decode_splitk_multi(
+    const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+    const float* v_scale, int32_t kv_dtype, const int32_t* page_table, int64_t page_table_stride,
+    const int32_t* cache_seqlens, const int32_t* cu_seqlens_q, int32_t bs, int32_t max_q_len,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+    int64_t num_pages, int32_t max_seq_pages, int32_t num_splits, float sm_scale,
+    float* scratch_m, float* scratch_l, float* scratch_acc, void* stream, int32_t use_pdl);
+
+/*
  * pa_reduce -- the log-sum-exp reducer (the standard and quantized reducer paths of
  * lmdeploy PR #4861 read the same fp32 partials, so one reducer serves both KV types):
  *   M = max_s m_s;  L = sum_s l_s exp(m_s - M)

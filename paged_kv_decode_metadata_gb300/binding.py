@@ -90,6 +90,9 @@ def _declare(lib):
                                            i32, i32, i32, vp, i32]
     lib.pa_decode_splitk.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, i32, i32, i32, i32,
                                      i32, i64, i32, i32, f32, vp, vp, vp, vp, i32]
+    lib.pa_decode_splitk_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, vp, i32, i32,
+                                           i32, i32, i32, i32, i64, i32, i32, f32, vp, vp, vp,
+                                           vp, i32]
     lib.pa_reduce.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32]
     lib.pa_decode_step.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp, vp, vp, i64,
                                    vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
@@ -110,7 +113,8 @@ def _declare(lib):
     lib.pa_status_string.argtypes = [i32]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_read_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
-    for name in ("pa_build_metadata", "pa_build_metadata_full", "pa_decode_splitk", "pa_reduce",
+    for name in ("pa_build_metadata", "pa_build_metadata_full", "pa_decode_splitk",
+                 "pa_decode_splitk_multi", "pa_reduce",
                  "pa_decode_step", "pa_read_error_flags"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
@@ -236,6 +240,28 @@ def pa_decode_splitk(q, k_cache, v_cache, page_table, cache_seqlens, scratch_m, 
         _ptr(scratch_m, torch.float32, "scratch_m"), _ptr(scratch_l, torch.float32, "scratch_l"),
         _ptr(scratch_acc, torch.float32, "scratch_acc"), _stream(stream), int(bool(use_pdl)))
     _check("pa_decode_splitk", st)
+
+
+def pa_decode_splitk_multi(q, k_cache, v_cache, page_table, cache_seqlens, cu_seqlens_q,
+                           scratch_m, scratch_l, scratch_acc, *, max_q_len: int,
+                           max_seq_pages: int, num_splits: int, sm_scale: float, k_scale=None,
+                           v_scale=None, stream=None, use_pdl: bool = True):
+    """Split-K producer for several query tokens per request (rows from cu_seqlens_q,
+    causal within the request's newest tokens); see include/pa.h."""
+    lib = load()
+    kv_dtype, ks, vs = _kv_args(k_cache, v_cache, k_scale, v_scale)
+    total_q, hq, d = q.shape
+    bs = cache_seqlens.shape[0]
+    num_pages, hkv, page_size, _ = k_cache.shape
+    st = lib.pa_decode_splitk_multi(
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
+        ks, vs, kv_dtype, _ptr2d(page_table, torch.int32, "page_table"),
+        _row_stride(page_table, "page_table"), _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
+        _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q"), bs, int(max_q_len), hq, hkv, d,
+        page_size, num_pages, int(max_seq_pages), int(num_splits), float(sm_scale),
+        _ptr(scratch_m, torch.float32, "scratch_m"), _ptr(scratch_l, torch.float32, "scratch_l"),
+        _ptr(scratch_acc, torch.float32, "scratch_acc"), _stream(stream), int(bool(use_pdl)))
+    _check("pa_decode_splitk_multi", st)
 
 
 def pa_reduce(scratch_m, scratch_l, scratch_acc, out, lse=None, *, stream=None,

@@ -214,14 +214,19 @@ pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_t* seq_
       PA_Q_MODE_NONE, 0, stream, use_pdl);
 }
 
-pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
-                           const float* k_scale, const float* v_scale, int32_t kv_dtype,
-                           const int32_t* page_table, int64_t page_table_stride,
-                           const int32_t* cache_seqlens, int32_t bs, int32_t num_q_heads,
-                           int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
-                           int64_t num_pages, int32_t max_seq_pages, int32_t num_splits,
-                           float sm_scale, float* scratch_m, float* scratch_l,
-                           float* scratch_acc, void* stream, int32_t use_pdl) {
+}  // extern "C"
+
+namespace {
+
+pa_status decode_splitk_impl(const void* q, const void* k_cache, const void* v_cache,
+                             const float* k_scale, const float* v_scale, int32_t kv_dtype,
+                             const int32_t* page_table, int64_t page_table_stride,
+                             const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
+                             int32_t max_q_len, int32_t bs, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                             int64_t num_pages, int32_t max_seq_pages, int32_t num_splits,
+                             float sm_scale, float* scratch_m, float* scratch_l,
+                             float* scratch_acc, void* stream, int32_t use_pdl) {
   pa_status st = check_attention(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
                                  page_table_stride, cache_seqlens, bs, num_q_heads,
                                  num_kv_heads, head_dim, page_size, num_pages, max_seq_pages,
@@ -231,6 +236,10 @@ pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cac
     return PA_ERR_INVALID;
   const int group = num_q_heads / num_kv_heads;
   const bool use_fma = g_producer.load() == PA_PRODUCER_FMA;
+  if (cu_seqlens_q != nullptr) {
+    if (max_q_len < 1) return PA_ERR_INVALID;
+    if (use_fma || static_cast<int64_t>(group) * max_q_len > 16) return PA_ERR_UNSUPPORTED;
+  }
   if (use_fma && group > 8) return PA_ERR_UNSUPPORTED;
   pa::SplitKParams p = {};
   p.q = q;
@@ -248,6 +257,8 @@ pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cac
   p.pages_per_split = static_cast<int32_t>(cdiv(max_seq_pages, num_splits));
   p.num_splits = num_splits;
   p.q_scale = sm_scale * 1.4426950408889634f;  // log2(e): the kernel works in base 2
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.max_q_len = cu_seqlens_q != nullptr ? max_q_len : 1;
   p.m_out = scratch_m;
   p.l_out = scratch_l;
   p.acc_out = scratch_acc;
@@ -264,6 +275,42 @@ pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cac
   }
   if (e == cudaSuccess) e = pa::fail_at(cudaGetLastError(), "error state after launch");
   return from_cuda(e, "split-K producer launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cache,
+                           const float* k_scale, const float* v_scale, int32_t kv_dtype,
+                           const int32_t* page_table, int64_t page_table_stride,
+                           const int32_t* cache_seqlens, int32_t bs, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                           int64_t num_pages, int32_t max_seq_pages, int32_t num_splits,
+                           float sm_scale, float* scratch_m, float* scratch_l,
+                           float* scratch_acc, void* stream, int32_t use_pdl) {
+  return decode_splitk_impl(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
+                            page_table_stride, cache_seqlens, nullptr, 1, bs, num_q_heads,
+                            num_kv_heads, head_dim, page_size, num_pages, max_seq_pages,
+                            num_splits, sm_scale, scratch_m, scratch_l, scratch_acc, stream,
+                            use_pdl);
+}
+
+pa_status pa_decode_splitk_multi(const void* q, const void* k_cache, const void* v_cache,
+                                 const float* k_scale, const float* v_scale, int32_t kv_dtype,
+                                 const int32_t* page_table, int64_t page_table_stride,
+                                 const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
+                                 int32_t bs, int32_t max_q_len, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                 int64_t num_pages, int32_t max_seq_pages, int32_t num_splits,
+                                 float sm_scale, float* scratch_m, float* scratch_l,
+                                 float* scratch_acc, void* stream, int32_t use_pdl) {
+  if (cu_seqlens_q == nullptr) return PA_ERR_INVALID;
+  return decode_splitk_impl(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
+                            page_table_stride, cache_seqlens, cu_seqlens_q, max_q_len, bs,
+                            num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                            max_seq_pages, num_splits, sm_scale, scratch_m, scratch_l,
+                            scratch_acc, stream, use_pdl);
 }
 
 pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const float* scratch_acc,

@@ -53,6 +53,11 @@ struct SplitKParams {
   int32_t pages_per_split;
   int32_t num_splits;
   float q_scale;  // sm_scale * log2(e)
+  // Several query tokens per request (tensor-core producer only): query rows of request
+  // b are cu_seqlens_q[b] .. cu_seqlens_q[b+1], at most max_q_len of them; nullptr for
+  // one query per request (row b).
+  const int32_t* cu_seqlens_q;
+  int32_t max_q_len;
   float* m_out;
   float* l_out;
   float* acc_out;

@@ -152,25 +152,30 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// B operand of S^T = K Q^T for request b, kv head kvh: b0 = Q[head][k 2tig, 2tig+1],
-// b1 = Q[head][k 2tig+8, +9] of k-step j, head = 8 * nt + gid (zero for heads >= G).
-// int8 path (kF16): fp16 Q in the permuted contraction order (k-step j, lane tig ->
-// channels 32*tig + 4*j + {0..3}), plus kbias: the K codes enter the MMA biased by
-// +1152 (the widening skips the subtract), so each score carries 1152 * sum_d q[h][d];
-// kbias[nt][e] (head 8nt + 2tig + e) is that offset from the same fp16 Q values.
+// B operand of S^T = K Q^T.  Column n of the N dimension is query i = n / G of the
+// request (row q_begin + i) and query head kvh * G + n % G; columns n >= q_len * G are
+// zero.  b0 = Q[col][k 2tig, 2tig+1], b1 = Q[col][k 2tig+8, +9] of k-step j, for
+// column n = 8 * nt + gid.  int8 path (kF16): fp16 Q in the permuted contraction order
+// (k-step j, lane tig -> channels 32*tig + 4*j + {0..3}), plus kbias: the K codes enter
+// the MMA biased by +1152 (the widening skips the subtract), so each score carries
+// 1152 * sum_d q[col][d]; kbias[nt][e] (column 8nt + 2tig + e) is that offset from the
+// same fp16 Q values.  The whole warp calls this.
 template <bool kF16, int kNT>
-__device__ __forceinline__ void load_q_fragments(const SplitKParams& prm, int b, int kvh, int G,
-                                                 int gid, int tig, uint32_t (&qb)[kNT][8][2],
+__device__ __forceinline__ void load_q_fragments(const SplitKParams& prm, int q_begin, int q_len,
+                                                 int kvh, int G, int gid, int tig,
+                                                 uint32_t (&qb)[kNT][8][2],
                                                  float (&kbias)[kNT][2]) {
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) {
-    const int head = 8 * nt + gid;
+    const int col = 8 * nt + gid;
+    const int qi = col / G;
+    const int head = kvh * G + (col - qi * G);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       uint32_t lo = 0, hi = 0;
-      if (head < G) {
+      if (col < q_len * G) {
         const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(prm.q) +
-                                  (static_cast<int64_t>(b) * prm.num_q_heads + kvh * G + head) * 128;
+                                  (static_cast<int64_t>(q_begin + qi) * prm.num_q_heads + head) * 128;
         if constexpr (kF16) {
           const int d = 32 * tig + 4 * j;
           lo = pack_f16(__bfloat162float(qr[d]), __bfloat162float(qr[d + 1]));
@@ -194,11 +199,19 @@ __device__ __forceinline__ void load_q_fragments(const SplitKParams& prm, int b,
         part += (a.x + a.y) + (c.x + c.y);
       }
       part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);  // sum over the head's 128 channels
+      part += __shfl_xor_sync(0xffffffffu, part, 2);  // sum over the column's 128 channels
       kbias[nt][0] = 1152.f * __shfl_sync(0xffffffffu, part, (2 * tig) * 4);
       kbias[nt][1] = 1152.f * __shfl_sync(0xffffffffu, part, (2 * tig + 1) * 4);
     }
   }
+}
+
+// Scratch slot of column `col` (query col / G, head col % G of kv head kvh) for `split`.
+__device__ __forceinline__ int64_t column_slot(int q_begin, int col, int G, int kvh,
+                                               int num_q_heads, int S, int split) {
+  const int qi = col / G;
+  return ((static_cast<int64_t>(q_begin) + qi) * num_q_heads + kvh * G + (col - qi * G)) * S +
+         split;
 }
 
 template <bool kQuant, int P, int STAGES, int MINB, int kNT>
@@ -227,10 +240,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC);
 
   // ---- prologue independent of the metadata stage: Q^T fragments in registers ------
+  // (with several queries per request their rows come from cu_seqlens_q, a metadata
+  // output, so Q is loaded after the wait instead)
   const int b = blockIdx.z;
+  const bool multi = prm.cu_seqlens_q != nullptr;
   uint32_t qb[kNT][8][2];
   float kbias[kNT][2];
-  if (is_consumer) load_q_fragments<kF16, kNT>(prm, b, kvh, G, gid, tig, qb, kbias);
+  if (!multi && is_consumer) load_q_fragments<kF16, kNT>(prm, b, 1, kvh, G, gid, tig, qb, kbias);
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -245,6 +261,18 @@ __global__ void __launch_bounds__(kThreads, MINB)
   PA_TS_FIRST(prm.ts, 1, kTsReady);
 
 
+  int q_begin = b, q_len = 1;
+  if (multi) {
+    q_begin = prm.cu_seqlens_q[b];
+    q_len = prm.cu_seqlens_q[b + 1] - q_begin;
+    if (q_len < 0 || q_len > prm.max_q_len) {
+      if (tid == 0 && split == 0 && kvh == 0) record_error(prm.err, kErrSeqLenOutOfRange);
+      q_len = q_len < 0 ? 0 : prm.max_q_len;
+    }
+    if (is_consumer) load_q_fragments<kF16, kNT>(prm, q_begin, q_len, kvh, G, gid, tig, qb, kbias);
+  }
+  const int ncols = q_len * G;  // (query, head) columns of this request and kv head
+
   int n = prm.cache_seqlens[b];
   const int cap = prm.max_seq_pages * P;
   if (n < 0 || n > cap) {
@@ -256,14 +284,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const int p_end = min(p_begin + prm.pages_per_split, n_pages);
   const int tok_begin = p_begin * P;
   const int n_tok = min(p_end * P, n) - tok_begin;
-  const int64_t slot0 =
-      (static_cast<int64_t>(b) * prm.num_q_heads + kvh * G) * S + split;
 
   if (n_tok <= 0) {
     trigger_dependents();
-    if (tid < G) {
-      prm.m_out[slot0 + static_cast<int64_t>(tid) * S] = -CUDART_INF_F;
-      prm.l_out[slot0 + static_cast<int64_t>(tid) * S] = 0.f;
+    if (tid < ncols) {
+      const int64_t slot = column_slot(q_begin, tid, G, kvh, prm.num_q_heads, S, split);
+      prm.m_out[slot] = -CUDART_INF_F;
+      prm.l_out[slot] = 0.f;
     }
     PA_TS_LAST(prm.ts, 1);
     return;
@@ -382,6 +409,17 @@ __global__ void __launch_bounds__(kThreads, MINB)
   const float q_scale = prm.q_scale;
   const int t0 = warp * 16;  // this warp's tokens inside every chunk
   bool failed = false;
+  // Causal limit of this thread's columns, in token positions of the split: query i of a
+  // request with q_len queries sees positions < n - q_len + i + 1 (its own token is the
+  // request's (q_len - i)-th newest).  One query per request: the whole context.
+  int lim[kNT][2];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = 8 * nt + 2 * tig + e;
+      lim[nt][e] = col < ncols ? n - q_len + col / G + 1 - tok_begin : 0;
+    }
 
   for (int c = 0; c < n_chunks; ++c) {
     const int stage = c % STAGES;
@@ -476,7 +514,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
           if constexpr (kQuant) v -= kbias[nt][i & 1];
           v *= q_scale;
           if constexpr (kQuant) v *= (i < 2 ? ks_a : ks_b);
-          x[i] = (i < 2 ? tok_a : tok_b) < valid ? v : -CUDART_INF_F;
+          const int pos = c * kChunk + (i < 2 ? tok_a : tok_b);  // position in the split
+          x[i] = ((i < 2 ? tok_a : tok_b) < valid && pos < lim[nt][i & 1]) ? v : -CUDART_INF_F;
         }
         float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
@@ -608,8 +647,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
   for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int head = 8 * nt + 2 * tig + e;
-      if (head < G) {
+      const int head = 8 * nt + 2 * tig + e;  // column
+      if (head < ncols) {
         float mrow = -CUDART_INF_F;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + head) * 2]);
@@ -625,18 +664,18 @@ __global__ void __launch_bounds__(kThreads, MINB)
       }
     }
   consumer_barrier();
-  for (int idx = tid; idx < G * 32; idx += kConsumerWarps * 32) {
-    const int head = idx >> 5, d = (idx & 31) * 4;
+  for (int idx = tid; idx < ncols * 32; idx += kConsumerWarps * 32) {
+    const int head = idx >> 5, d = (idx & 31) * 4;  // column, channel
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
       const float4 v = *reinterpret_cast<const float4*>(red + (w * 16 + head) * 128 + d);
       sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
     }
-    *reinterpret_cast<float4*>(prm.acc_out + (slot0 + static_cast<int64_t>(head) * S) * 128 + d) =
-        sum;
+    *reinterpret_cast<float4*>(
+        prm.acc_out + column_slot(q_begin, head, G, kvh, prm.num_q_heads, S, split) * 128 + d) = sum;
   }
-  if (tid < G) {
+  if (tid < ncols) {
     float mrow = -CUDART_INF_F;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + tid) * 2]);
@@ -646,8 +685,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const float mw = ml_s[(w * 16 + tid) * 2];
       if (mw != -CUDART_INF_F) lsum += ml_s[(w * 16 + tid) * 2 + 1] * exp2f(mw - mrow);
     }
-    prm.m_out[slot0 + static_cast<int64_t>(tid) * S] = mrow * 0.69314718055994530942f;
-    prm.l_out[slot0 + static_cast<int64_t>(tid) * S] = lsum;
+    const int64_t slot = column_slot(q_begin, tid, G, kvh, prm.num_q_heads, S, split);
+    prm.m_out[slot] = mrow * 0.69314718055994530942f;
+    prm.l_out[slot] = lsum;
   }
   PA_TS_LAST(prm.ts, 1);
 }
@@ -731,7 +771,7 @@ cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_s
   if (e != cudaSuccess) return fail_at(e, "tensor map encode (V)");
   const dim3 grid(static_cast<unsigned>(p.num_splits), static_cast<unsigned>(p.num_kv_heads),
                   static_cast<unsigned>(bs));
-  const bool two_tiles = group > 8;
+  const bool two_tiles = group * (p.cu_seqlens_q != nullptr ? p.max_q_len : 1) > 8;
 #define PA_MMA_CASE(PP)                                                                        \
   if (page_size == PP) {                                                                       \
     return two_tiles                                                                           \
