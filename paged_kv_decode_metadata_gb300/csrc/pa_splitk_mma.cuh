@@ -273,6 +273,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
   }
   const int ncols = q_len * G;  // (query, head) columns of this request and kv head
 
+  // The split's page indices and the request length are independent loads: issue both
+  // before either is used (page indices are bounds-checked where they are used).
+  const int p_begin = split * prm.pages_per_split;
+  const int32_t* pt_row =
+      prm.page_table + static_cast<int64_t>(b) * prm.page_table_stride + p_begin;
+  const int pages_cap = min(min(prm.pages_per_split, prm.max_seq_pages - p_begin), kMaxSplitPages);
+  for (int i = tid; i < pages_cap; i += kThreads) pages_s[i] = pt_row[i];
   int n = prm.cache_seqlens[b];
   const int cap = prm.max_seq_pages * P;
   if (n < 0 || n > cap) {
@@ -280,7 +287,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
     n = n < 0 ? 0 : cap;
   }
   const int n_pages = (n + P - 1) / P;
-  const int p_begin = split * prm.pages_per_split;
   const int p_end = min(p_begin + prm.pages_per_split, n_pages);
   const int tok_begin = p_begin * P;
   const int n_tok = min(p_end * P, n) - tok_begin;
@@ -297,16 +303,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
   }
 
   const int n_split_pages = p_end - p_begin;
-  const int32_t* pt_row =
-      prm.page_table + static_cast<int64_t>(b) * prm.page_table_stride + p_begin;
-  for (int i = tid; i < min(n_split_pages, kMaxSplitPages); i += kThreads) {
-    int32_t pg = pt_row[i];
-    if (pg < 0 || pg >= prm.num_pages) {
-      record_error(prm.err, kErrPageOutOfRange);
-      pg = 0;
-    }
-    pages_s[i] = pg;
-  }
   __syncthreads();  // barriers initialised, page indices cached
 
   const int n_chunks = (n_tok + kChunk - 1) / kChunk;
@@ -329,8 +325,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const uint32_t vdst = kdst + L::KV_BYTES;
         const int ctok = c * kChunk;
         auto page_at = [&](int i) -> int {
-          if (i < kMaxSplitPages) return pages_s[i];
-          int32_t pg = pt_row[i];
+          int32_t pg = i < kMaxSplitPages ? pages_s[i] : pt_row[i];
           if (pg < 0 || pg >= prm.num_pages) {
             record_error(prm.err, kErrPageOutOfRange);
             pg = 0;
