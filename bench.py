@@ -487,10 +487,11 @@ def run_gb300(args, spec, rank, world, local_rank):
 
 
 def run_table(args):
-    """Per-workload latency table (graph replay with and without PDL, eager with PDL),
-    KV bandwidth against the measured peak.  L2: workloads whose inputs fit in the
-    129 MB L2 are also timed rotating over enough copies of the inputs to exceed 2x L2
-    (one CUDA graph per copy, replayed round-robin)."""
+    """Per-workload latency table: CUDA graphs holding 8 consecutive steps (so the time
+    per step is the GPU's, not the host's graph-launch rate), with and without PDL, and
+    eager C-ABI calls with PDL; KV bandwidth against the measured peak.  Workloads whose
+    per-step bytes fit in 2x the 129 MB L2 are also timed with the inputs rotated over
+    enough copies to exceed 2x L2 (one graph stepping through every copy in turn)."""
     import torch
 
     from paged_kv_decode_metadata_gb300 import binding, synthetic
@@ -503,17 +504,22 @@ def run_table(args):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     stream = torch.cuda.Stream()
     l2_bytes = torch.cuda.get_device_properties(0).L2_cache_size
+    per_graph = 8
     for name in synthetic.WORKLOAD_ORDER:
         wl = synthetic.make(synthetic.WORKLOADS[name])
         ds = DeviceStep(wl)
-        row = {"workload": name, "num_splits": ds.num_splits}
-        n = max(200, min(args.steps, 2000))
+        row = {"workload": name, "num_splits": ds.num_splits, "steps_per_graph": per_graph}
+        reps = max(20, min(args.steps, 2000) // per_graph)
         for pdl in (False, True):
-            g = capture(torch, lambda: ds.step(use_pdl=pdl), stream)
-            time_graph(torch, g, 50, stream)
-            row["graph_pdl_us" if pdl else "graph_us"] = min(time_graph(torch, g, n, stream)
-                                                            for _ in range(3))
+            def steps(pdl=pdl):
+                for _ in range(per_graph):
+                    ds.step(use_pdl=pdl)
+            g = capture(torch, steps, stream)
+            time_graph(torch, g, 5, stream)
+            row["graph_pdl_us" if pdl else "graph_us"] = min(
+                time_graph(torch, g, reps, stream) for _ in range(3)) / per_graph
             del g
+        n = max(200, min(args.steps, 2000))
         with torch.cuda.stream(stream):
             for _ in range(20):
                 ds.step(use_pdl=True)
@@ -527,22 +533,18 @@ def run_table(args):
         footprint = ds.step_bytes(wl.ctx)
         if footprint < 2 * l2_bytes:
             copies = int(2 * l2_bytes // footprint) + 1
-            steps = [ds] + [DeviceStep(wl) for _ in range(copies - 1)]
-            graphs = [capture(torch, lambda d=d: d.step(use_pdl=True), stream) for d in steps]
-            with torch.cuda.stream(stream):
-                for g in graphs:
-                    g.replay()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                reps = max(1, n // copies)
-                for _ in range(reps):
-                    for g in graphs:
-                        g.replay()
-                b.record(stream)
-            b.synchronize()
-            row["graph_pdl_l2_rotated_us"] = a.elapsed_time(b) / (reps * copies) * 1e3
+            others = [DeviceStep(wl) for _ in range(copies - 1)]
+            everyone = [ds] + others
+
+            def rotate():
+                for d in everyone:
+                    d.step(use_pdl=True)
+            g = capture(torch, rotate, stream)
+            time_graph(torch, g, 2, stream)
+            row["graph_pdl_l2_rotated_us"] = min(
+                time_graph(torch, g, max(5, reps // copies), stream) for _ in range(3)) / copies
             row["l2_rotation_copies"] = copies
-            del graphs, steps
+            del g, others, everyone
         best = row.get("graph_pdl_l2_rotated_us", row["graph_pdl_us"])
         row["kv_bytes"] = ds.kv_bytes(wl.ctx)
         row["step_bytes"] = footprint

@@ -54,6 +54,9 @@ constexpr int kChunk = 64;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSplitPages = 256;
+// Online-softmax slack (log2 units): the reference maximum of a column moves only when a
+// score exceeds it by more than this, so softmax weights stay below 2^8.
+constexpr float kMaxSlack = 8.f;
 
 template <bool kQuant, int STAGES>
 struct Layout {
@@ -64,8 +67,8 @@ struct Layout {
   static constexpr int OFF_PAGES = STAGES * STAGE_BYTES;
   static constexpr int OFF_FULL = OFF_PAGES + kMaxSplitPages * 4;
   static constexpr int OFF_EMPTY = OFF_FULL + STAGES * 8;
-  static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;                    // [4 warps][16 rows][2]
-  static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 2 * 4;    // abort flag
+  static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;      // [4 warps][16 columns][3]
+  static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 3 * 4;    // abort flag
   static constexpr int SMEM = OFF_MISC + 16 + 1024;                         // + alignment slack
   static constexpr int RED_BYTES = kConsumerWarps * 16 * 128 * 4;           // output merge buffer
   static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "merge buffer reuses the ring");
@@ -395,10 +398,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
   // softmax state of heads 8*nt + 2*tig + e (identical in the 8 lanes sharing tig)
-  float m_run[kNT][2], l_part[kNT][2];
+  // m_run: the reference maximum the weights are relative to (warp-uniform per column);
+  // t_max: this thread's true maximum of its own scores, reduced once per split.
+  float m_run[kNT][2], l_part[kNT][2], t_max[kNT][2];
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) {
     m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
+    t_max[nt][0] = t_max[nt][1] = -CUDART_INF_F;
     l_part[nt][0] = l_part[nt][1] = 0.f;
   }
   const float q_scale = prm.q_scale;
@@ -512,35 +518,45 @@ __global__ void __launch_bounds__(kThreads, MINB)
           const int pos = c * kChunk + (i < 2 ? tok_a : tok_b);  // position in the split
           x[i] = ((i < 2 ? tok_a : tok_b) < valid && pos < lim[nt][i & 1]) ? v : -CUDART_INF_F;
         }
+        // Reference maximum per column, moved only when a score exceeds it by more than
+        // 2^kMaxSlack (one vote instead of a shuffle reduction and a rescale per slice);
+        // weights stay <= 2^kMaxSlack and (m, l, acc) stay consistent for any reference.
         float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+        t_max[nt][0] = fmaxf(t_max[nt][0], mx0);
+        t_max[nt][1] = fmaxf(t_max[nt][1], mx1);
+        float alpha[2] = {1.f, 1.f}, p[4];
+        const bool grow = mx0 > m_run[nt][0] + kMaxSlack || mx1 > m_run[nt][1] + kMaxSlack;
+        if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-        for (int m = 4; m <= 16; m <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, m));
+          for (int m = 4; m <= 16; m <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, m));
+          }
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float m_new = fmaxf(m_run[nt][e], e == 0 ? mx0 : mx1);
+            if (m_new != -CUDART_INF_F) {
+              alpha[e] = exp2f(m_run[nt][e] - m_new);
+              m_run[nt][e] = m_new;
+            }
+          }
+          if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              o[nt][i][0] *= alpha[0];
+              o[nt][i][1] *= alpha[1];
+              o[nt][i][2] *= alpha[0];
+              o[nt][i][3] *= alpha[1];
+            }
+          }
         }
-        float alpha[2], p[4];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float m_new = fmaxf(m_run[nt][e], e == 0 ? mx0 : mx1);
-          if (m_new == -CUDART_INF_F) {
-            alpha[e] = 1.f;
-            p[e] = p[2 + e] = 0.f;
-          } else {
-            alpha[e] = exp2f(m_run[nt][e] - m_new);
-            p[e] = exp2f(x[e] - m_new);
-            p[2 + e] = exp2f(x[2 + e] - m_new);
-          }
+          // a column with no score yet (reference -inf) has only -inf scores here
+          const float ref = m_run[nt][e] == -CUDART_INF_F ? 0.f : m_run[nt][e];
+          p[e] = exp2f(x[e] - ref);
+          p[2 + e] = exp2f(x[2 + e] - ref);
           l_part[nt][e] = l_part[nt][e] * alpha[e] + (p[e] + p[2 + e]);
-          m_run[nt][e] = m_new;
-        }
-        if (alpha[0] != 1.f || alpha[1] != 1.f) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            o[nt][i][0] *= alpha[0];
-            o[nt][i][1] *= alpha[1];
-            o[nt][i][2] *= alpha[0];
-            o[nt][i][3] *= alpha[1];
-          }
         }
         // P^T as the B operand of O^T += V^T P^T: transpose the two 8x8 (token, head)
         // blocks in registers.
@@ -607,15 +623,22 @@ __global__ void __launch_bounds__(kThreads, MINB)
   trigger_dependents();
 
   // ---- merge the four warps' softmax states, write the split's partials -------------
+  // Per column: M = the split's true maximum (over warps of the lane-reduced t_max);
+  // warp w's weights are relative to its reference m_w <= M, so its sum and output
+  // are scaled by 2^(m_w - M).
   float l_head[kNT][2];
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      float v = l_part[nt][e];
+      float v = l_part[nt][e], t = t_max[nt][e];
 #pragma unroll
-      for (int m = 4; m <= 16; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+      for (int m = 4; m <= 16; m <<= 1) {
+        v += __shfl_xor_sync(0xffffffffu, v, m);
+        t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, m));
+      }
       l_head[nt][e] = v;
+      t_max[nt][e] = t;
     }
   if (gid == 0) {
 #pragma unroll
@@ -623,8 +646,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int head = 8 * nt + 2 * tig + e;
-        ml_s[(warp * 16 + head) * 2 + 0] = m_run[nt][e];
-        ml_s[(warp * 16 + head) * 2 + 1] = l_head[nt][e];
+        ml_s[(warp * 16 + head) * 3 + 0] = m_run[nt][e];
+        ml_s[(warp * 16 + head) * 3 + 1] = l_head[nt][e];
+        ml_s[(warp * 16 + head) * 3 + 2] = t_max[nt][e];
       }
   }
   consumer_barrier();
@@ -646,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       if (head < ncols) {
         float mrow = -CUDART_INF_F;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + head) * 2]);
+        for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + head) * 3 + 2]);
         const float scale = m_run[nt][e] == -CUDART_INF_F ? 0.f : exp2f(m_run[nt][e] - mrow);
         float* dst = red + (warp * 16 + head) * 128;
 #pragma unroll
@@ -673,12 +697,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
   if (tid < ncols) {
     float mrow = -CUDART_INF_F;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + tid) * 2]);
+    for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + tid) * 3 + 2]);
     float lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float mw = ml_s[(w * 16 + tid) * 2];
-      if (mw != -CUDART_INF_F) lsum += ml_s[(w * 16 + tid) * 2 + 1] * exp2f(mw - mrow);
+      const float mw = ml_s[(w * 16 + tid) * 3];
+      if (mw != -CUDART_INF_F) lsum += ml_s[(w * 16 + tid) * 3 + 1] * exp2f(mw - mrow);
     }
     const int64_t slot = column_slot(q_begin, tid, G, kvh, prm.num_q_heads, S, split);
     prm.m_out[slot] = mrow * 0.69314718055994530942f;

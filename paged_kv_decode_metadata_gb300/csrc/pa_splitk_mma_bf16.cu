@@ -3,12 +3,18 @@
 
 namespace pa {
 
-#ifndef PA_MMA_BF16_STAGES1
 // G <= 8: two 32 KiB stages (K + V of a 64-token chunk) per CTA, three CTAs per SM.
 // G = 16: three stages, two CTAs per SM (twice the output fragments per thread).
+#ifndef PA_MMA_BF16_STAGES1
 #define PA_MMA_BF16_STAGES1 2
+#endif
+#ifndef PA_MMA_BF16_MINB1
 #define PA_MMA_BF16_MINB1 3
+#endif
+#ifndef PA_MMA_BF16_STAGES2
 #define PA_MMA_BF16_STAGES2 3
+#endif
+#ifndef PA_MMA_BF16_MINB2
 #define PA_MMA_BF16_MINB2 2
 #endif
 

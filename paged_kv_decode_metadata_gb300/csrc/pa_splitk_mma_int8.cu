@@ -3,12 +3,18 @@
 
 namespace pa {
 
-#ifndef PA_MMA_INT8_STAGES1
 // G <= 8: four 17 KiB stages (codes and scales of a 64-token chunk) per CTA, three CTAs
 // per SM.  G = 16: six stages, two CTAs per SM.
+#ifndef PA_MMA_INT8_STAGES1
 #define PA_MMA_INT8_STAGES1 4
+#endif
+#ifndef PA_MMA_INT8_MINB1
 #define PA_MMA_INT8_MINB1 3
+#endif
+#ifndef PA_MMA_INT8_STAGES2
 #define PA_MMA_INT8_STAGES2 6
+#endif
+#ifndef PA_MMA_INT8_MINB2
 #define PA_MMA_INT8_MINB2 2
 #endif
 
