@@ -56,7 +56,10 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSplitPages = 256;
 // Online-softmax slack (log2 units): the reference maximum of a column moves only when a
 // score exceeds it by more than this, so softmax weights stay below 2^8.
-constexpr float kMaxSlack = 8.f;
+#ifndef PA_MAX_SLACK
+#define PA_MAX_SLACK 8
+#endif
+constexpr float kMaxSlack = PA_MAX_SLACK;
 
 template <bool kQuant, int STAGES>
 struct Layout {

@@ -93,8 +93,12 @@ def test_splitk_scratch_matches_oracle_partials(name, impl):
     full = ~empty
     assert np.abs(m[full] - m_ref[full]).max() <= 1e-4 * max(1.0, np.abs(m_ref[full]).max())
     assert np.all(np.abs(l[full] - l_ref[full]) <= 1e-4 * l_ref[full])
+    # acc = sum_j p_j v_j with each weight p_j rounded once to bf16 (relative error
+    # <= 2^-9; the weights are relative to a reference maximum that may sit below the
+    # true one, so the largest weight need not be the exactly representable 1) and
+    # summed in fp32: |error| <= 2^-9 * sum_j p_j |v_j| + fp32 terms.
     vmax = float(wl.v_cache.float().abs().max())
-    tol = 2e-4 * l_ref[full][:, None] * vmax + 1e-6
+    tol = (2.0 ** -9 + 1e-5) * l_ref[full][:, None] * vmax + 1e-6
     assert np.all(np.abs(acc[full] - acc_ref[full]) <= tol)
 
 
