@@ -78,10 +78,16 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                                  i32, i32, i32, i32, f64, vp, vp]
     lib.oracle_splitk_partials.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, i32, i32,
                                            i32, i32, i32, i32, i32, f64, vp, vp, vp]
+    lib.oracle_paged_attention_window.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, vp,
+                                                  i32, i32, i32, i32, i32, i32, f64, vp, vp]
+    lib.oracle_splitk_partials_window.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, vp,
+                                                  i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                                  f64, vp, vp, vp]
     lib.oracle_combine_splits.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
     for name in ("oracle_build_metadata", "oracle_cu_seqlens_q", "oracle_swa_out_cache_loc",
                  "oracle_paged_attention", "oracle_paged_attention_multi",
-                 "oracle_splitk_partials", "oracle_combine_splits"):
+                 "oracle_splitk_partials", "oracle_combine_splits",
+                 "oracle_paged_attention_window", "oracle_splitk_partials_window"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -201,6 +207,51 @@ def paged_attention_multi(q_bits, k_cache, v_cache, page_table, cache_seqlens, c
                                      pt.shape[1], _p(cl), _p(cq), cl.shape[0], hq, hkv, d,
                                      page_size, float(sm_scale), _p(out), _p(lse))
     return out, lse
+
+
+def paged_attention_window(q_bits, k_cache, v_cache, page_table, cache_seqlens, window,
+                           sm_scale, cu_seqlens_q=None, k_scale=None, v_scale=None, lib=None):
+    """Sliding-window attention through a sliding-window page table (-1 pages skipped).
+
+    ``q_bits`` [rows, Hq, d] uint16: one row per request, or the rows ``cu_seqlens_q``
+    [bs + 1] int32 assigns.  ``k_cache``/``v_cache`` is the sliding-window pool.
+    Returns (out [rows, Hq, d], lse [rows, Hq]) in float64.
+    """
+    lib = lib or load()
+    q, k, v, ks, vs, kv_dtype = _attention_args(q_bits, k_cache, v_cache, k_scale, v_scale)
+    pt = _c(page_table, np.int32)
+    cl = _c(cache_seqlens, np.int32)
+    cq = _c(cu_seqlens_q, np.int32) if cu_seqlens_q is not None else None
+    rows, hq, d = q.shape
+    _, hkv, page_size, _ = k.shape
+    out = np.zeros((rows, hq, d), np.float64)
+    lse = np.zeros((rows, hq), np.float64)
+    lib.oracle_paged_attention_window(_p(q), _p(k), _p(v), _p(ks), _p(vs), kv_dtype, _p(pt),
+                                      pt.shape[1], _p(cl), _p(cq), cl.shape[0], hq, hkv, d,
+                                      page_size, int(window), float(sm_scale), _p(out), _p(lse))
+    return out, lse
+
+
+def splitk_partials_window(q_bits, k_cache, v_cache, page_table, cache_seqlens, window,
+                           sm_scale, max_seq_pages, num_splits, cu_seqlens_q=None,
+                           max_q_len=1, k_scale=None, v_scale=None, lib=None):
+    """Per-split (m, l, acc) of the sliding-window attention over the window's split
+    partition; shapes [rows,Hq,S], [rows,Hq,S], [rows,Hq,S,d] in float64."""
+    lib = lib or load()
+    q, k, v, ks, vs, kv_dtype = _attention_args(q_bits, k_cache, v_cache, k_scale, v_scale)
+    pt = _c(page_table, np.int32)
+    cl = _c(cache_seqlens, np.int32)
+    cq = _c(cu_seqlens_q, np.int32) if cu_seqlens_q is not None else None
+    rows, hq, d = q.shape
+    _, hkv, page_size, _ = k.shape
+    m = np.zeros((rows, hq, num_splits), np.float64)
+    l = np.zeros((rows, hq, num_splits), np.float64)
+    acc = np.zeros((rows, hq, num_splits, d), np.float64)
+    lib.oracle_splitk_partials_window(_p(q), _p(k), _p(v), _p(ks), _p(vs), kv_dtype, _p(pt),
+                                      pt.shape[1], _p(cl), _p(cq), cl.shape[0], int(max_q_len),
+                                      hq, hkv, d, page_size, int(max_seq_pages), int(window),
+                                      int(num_splits), float(sm_scale), _p(m), _p(l), _p(acc))
+    return m, l, acc
 
 
 def splitk_partials(q_bits, k_cache, v_cache, page_table, cache_seqlens, sm_scale,

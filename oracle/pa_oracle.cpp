@@ -21,9 +21,16 @@
 //   * oracle_paged_attention_multi - the same attention for several query tokens per
 //     request (rows given by cu_seqlens_q, the module's query-length output), causal
 //     within the request's newest tokens.
+//   * oracle_paged_attention_window - sliding-window attention through the SWA page
+//     table the metadata module builds (swa_page_table): each query sees only its
+//     `window` newest positions, read from the sliding-window pool, and skips pages
+//     whose table entry is -1.  The pages build the table but do not print the
+//     attention that reads it; the window reading is stated at the function.
 //   * oracle_splitk_partials  - the per-split partial results (running max m,
 //     sum of exponentials l, unnormalised accumulator acc) that the split-K
 //     producer writes to scratch, for a given split of the context.
+//   * oracle_splitk_partials_window - the same partials for the sliding-window
+//     attention, over the window's split partition.
 //   * oracle_combine_splits   - the log-sum-exp combination the reducer performs.
 //
 // Parity pins: every function here is checked by CPU tests against hand-worked
@@ -336,6 +343,172 @@ int oracle_splitk_partials(const uint16_t* q, const void* k_cache, const void* v
         }
         m_out[slot] = x_max;
         l_out[slot] = l;
+      }
+    }
+  }
+  return 0;
+}
+
+// Sliding-window attention through the sliding-window page table.
+// Request b has n = cache_seqlens[b] cached tokens and q_len query rows: rows
+// cu_seqlens_q[b] .. cu_seqlens_q[b+1] when cu_seqlens_q is given, else the single row b
+// (q_len = 1).  The queries are the request's newest tokens, so query i sits at position
+// pos = n - q_len + i and attends positions j with
+//   max(0, pos - window + 1) <= j <= pos          (its `window` newest positions)
+// whose page entry page_table[b, j / page_size] is >= 0 (a -1 entry is a page the
+// sliding-window pool does not hold: its tokens are skipped).  Token j is row
+// j % page_size of that page of the sliding-window pool (k/v laid out as for
+// oracle_paged_attention).  Scores, softmax, output and lse as in
+// oracle_paged_attention; a query with no visible token gets out = 0, lse = -inf.
+// out [rows][num_q_heads][head_dim], lse [rows][num_q_heads].
+int oracle_paged_attention_window(const uint16_t* q, const void* k_cache, const void* v_cache,
+                                  const float* k_scale, const float* v_scale, int32_t kv_dtype,
+                                  const int32_t* page_table, int64_t page_table_stride,
+                                  const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
+                                  int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t page_size, int32_t window,
+                                  double sm_scale, double* out, double* lse) {
+  const int32_t group = num_q_heads / num_kv_heads;
+  for (int32_t b = 0; b < bs; ++b) {
+    const int64_t q_begin = cu_seqlens_q != nullptr ? cu_seqlens_q[b] : b;
+    const int64_t q_len = cu_seqlens_q != nullptr ? cu_seqlens_q[b + 1] - q_begin : 1;
+    const int64_t n = cache_seqlens[b];
+    for (int64_t i = 0; i < q_len; ++i) {
+      const int64_t row = q_begin + i;
+      const int64_t pos = n - q_len + i;
+      const int64_t lo = pos - window + 1 > 0 ? pos - window + 1 : 0;
+      // the visible tokens and their pages
+      std::vector<int64_t> tok, pg;
+      for (int64_t j = lo; j <= pos; ++j) {
+        const int64_t page = page_table[b * page_table_stride + j / page_size];
+        if (page < 0) continue;
+        tok.push_back(j);
+        pg.push_back(page);
+      }
+      for (int32_t h = 0; h < num_q_heads; ++h) {
+        const int32_t kv_head = h / group;
+        const uint16_t* qrow = q + (row * num_q_heads + h) * head_dim;
+        double* orow = out + (row * num_q_heads + h) * head_dim;
+        for (int32_t c = 0; c < head_dim; ++c) orow[c] = 0.0;
+        if (tok.empty()) {
+          lse[row * num_q_heads + h] = -std::numeric_limits<double>::infinity();
+          continue;
+        }
+        std::vector<double> x(tok.size());
+        double x_max = -std::numeric_limits<double>::infinity();
+        for (size_t t = 0; t < tok.size(); ++t) {
+          const int32_t off = static_cast<int32_t>(tok[t] % page_size);
+          double dot = 0.0;
+          for (int32_t c = 0; c < head_dim; ++c) {
+            dot += bf16_bits_to_double(qrow[c]) *
+                   kv_element(k_cache, k_scale, kv_dtype, pg[t], kv_head, off, c,
+                              num_kv_heads, page_size, head_dim);
+          }
+          x[t] = sm_scale * dot;
+          if (x[t] > x_max) x_max = x[t];
+        }
+        double denom = 0.0;
+        for (size_t t = 0; t < tok.size(); ++t) denom += std::exp(x[t] - x_max);
+        for (size_t t = 0; t < tok.size(); ++t) {
+          const int32_t off = static_cast<int32_t>(tok[t] % page_size);
+          const double w = std::exp(x[t] - x_max) / denom;
+          for (int32_t c = 0; c < head_dim; ++c) {
+            orow[c] += w * kv_element(v_cache, v_scale, kv_dtype, pg[t], kv_head, off, c,
+                                      num_kv_heads, page_size, head_dim);
+          }
+        }
+        lse[row * num_q_heads + h] = x_max + std::log(denom);
+      }
+    }
+  }
+  return 0;
+}
+
+// Split partials of the sliding-window attention.  The splits cover the window of the
+// request rather than its whole context: with
+//   window_pages = min(max_seq_pages, (window + max_q_len - 2) / page_size + 2)
+// (the most pages that the positions any query of a request can see, at most
+// window + max_q_len - 1 consecutive ones, can touch) and
+//   split_tokens = page_size * ceil(window_pages / num_splits),
+// split s of request b covers positions
+//   [base + s * split_tokens, base + (s + 1) * split_tokens),
+//   base = page_size * floor(max(0, n - q_len - window + 1) / page_size),
+// i.e. the splits start at the page holding the first position the request's earliest
+// query sees.  Each query sees, within its split, the positions and pages
+// oracle_paged_attention_window lets it see; m, l, acc per (row, head, split) as in
+// oracle_splitk_partials.  Rows as in oracle_paged_attention_window (cu_seqlens_q or one
+// per request).
+int oracle_splitk_partials_window(const uint16_t* q, const void* k_cache, const void* v_cache,
+                                  const float* k_scale, const float* v_scale, int32_t kv_dtype,
+                                  const int32_t* page_table, int64_t page_table_stride,
+                                  const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
+                                  int32_t bs, int32_t max_q_len, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                  int32_t max_seq_pages, int32_t window, int32_t num_splits,
+                                  double sm_scale, double* m_out, double* l_out,
+                                  double* acc_out) {
+  const int32_t group = num_q_heads / num_kv_heads;
+  int64_t window_pages = (static_cast<int64_t>(window) + max_q_len - 2) / page_size + 2;
+  if (window_pages > max_seq_pages) window_pages = max_seq_pages;
+  const int64_t split_tokens = (window_pages + num_splits - 1) / num_splits * page_size;
+  for (int32_t b = 0; b < bs; ++b) {
+    const int64_t q_begin = cu_seqlens_q != nullptr ? cu_seqlens_q[b] : b;
+    const int64_t q_len = cu_seqlens_q != nullptr ? cu_seqlens_q[b + 1] - q_begin : 1;
+    const int64_t n = cache_seqlens[b];
+    const int64_t first = n - q_len - window + 1 > 0 ? n - q_len - window + 1 : 0;
+    const int64_t base = first / page_size * page_size;
+    for (int64_t i = 0; i < q_len; ++i) {
+      const int64_t row = q_begin + i;
+      const int64_t pos = n - q_len + i;
+      const int64_t lo = pos - window + 1 > 0 ? pos - window + 1 : 0;
+      for (int32_t h = 0; h < num_q_heads; ++h) {
+        const int32_t kv_head = h / group;
+        const uint16_t* qrow = q + (row * num_q_heads + h) * head_dim;
+        for (int32_t s = 0; s < num_splits; ++s) {
+          const int64_t slot = (row * num_q_heads + h) * num_splits + s;
+          double* acc = acc_out + slot * head_dim;
+          for (int32_t c = 0; c < head_dim; ++c) acc[c] = 0.0;
+          const int64_t begin = base + s * split_tokens;
+          const int64_t end = begin + split_tokens;
+          std::vector<int64_t> tok, pg;
+          for (int64_t j = begin; j < end; ++j) {
+            if (j < lo || j > pos) continue;
+            const int64_t page = page_table[b * page_table_stride + j / page_size];
+            if (page < 0) continue;
+            tok.push_back(j);
+            pg.push_back(page);
+          }
+          if (tok.empty()) {
+            m_out[slot] = -std::numeric_limits<double>::infinity();
+            l_out[slot] = 0.0;
+            continue;
+          }
+          std::vector<double> x(tok.size());
+          double x_max = -std::numeric_limits<double>::infinity();
+          for (size_t t = 0; t < tok.size(); ++t) {
+            const int32_t off = static_cast<int32_t>(tok[t] % page_size);
+            double dot = 0.0;
+            for (int32_t c = 0; c < head_dim; ++c) {
+              dot += bf16_bits_to_double(qrow[c]) *
+                     kv_element(k_cache, k_scale, kv_dtype, pg[t], kv_head, off, c,
+                                num_kv_heads, page_size, head_dim);
+            }
+            x[t] = sm_scale * dot;
+            if (x[t] > x_max) x_max = x[t];
+          }
+          double l = 0.0;
+          for (size_t t = 0; t < tok.size(); ++t) {
+            const int32_t off = static_cast<int32_t>(tok[t] % page_size);
+            const double w = std::exp(x[t] - x_max);
+            l += w;
+            for (int32_t c = 0; c < head_dim; ++c) {
+              acc[c] += w * kv_element(v_cache, v_scale, kv_dtype, pg[t], kv_head, off, c,
+                                       num_kv_heads, page_size, head_dim);
+            }
+          }
+          m_out[slot] = x_max;
+          l_out[slot] = l;
+        }
       }
     }
   }

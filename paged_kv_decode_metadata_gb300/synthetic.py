@@ -90,6 +90,12 @@ class Workload:
     full_to_swa_mapping: Optional[torch.Tensor]  # [num_pages*page_size + page_size + 1] int64
     swa_pages: Optional[list]      # per request: {page index in request: swa page}
     swa_window_start: Optional[list]  # per request: first in-window token position
+    swa_num_pages: int = 0         # pages of the sliding-window pool
+    # sliding-window pool (make(..., with_swa_cache=True)): same layouts as the full pool
+    k_swa: Optional[torch.Tensor] = None
+    v_swa: Optional[torch.Tensor] = None
+    k_swa_scale: Optional[torch.Tensor] = None
+    v_swa_scale: Optional[torch.Tensor] = None
 
     @property
     def sm_scale(self) -> float:
@@ -97,8 +103,27 @@ class Workload:
         return float(torch.tensor(self.spec.head_dim ** -0.5, dtype=torch.float32))
 
 
-def make(spec: Spec, seed: Optional[int] = None, with_cache: bool = True) -> Workload:
-    """Draw one workload.  ``with_cache=False`` skips the (large) K/V pools."""
+def _draw_cache(spec: Spec, num_pages: int, g: torch.Generator):
+    shape = (num_pages, spec.num_kv_heads, spec.page_size, spec.head_dim)
+    if spec.kv_dtype == "bf16":
+        k = torch.randn(shape, generator=g).to(torch.bfloat16)
+        v = torch.randn(shape, generator=g).to(torch.bfloat16)
+        return k, v, None, None
+    if spec.kv_dtype == "int8":
+        k = torch.randint(-127, 128, shape, generator=g, dtype=torch.int8)
+        v = torch.randint(-127, 128, shape, generator=g, dtype=torch.int8)
+        sshape = (num_pages, spec.num_kv_heads, spec.page_size)
+        ks = torch.rand(sshape, generator=g) * 0.045 + 0.005
+        vs = torch.rand(sshape, generator=g) * 0.045 + 0.005
+        return k, v, ks, vs
+    raise ValueError(spec.kv_dtype)
+
+
+def make(spec: Spec, seed: Optional[int] = None, with_cache: bool = True,
+         with_swa_cache: bool = False) -> Workload:
+    """Draw one workload.  ``with_cache=False`` skips the (large) K/V pools;
+    ``with_swa_cache`` also draws the sliding-window pool (after everything else, so
+    the other tensors do not depend on it)."""
     g = torch.Generator().manual_seed(spec.seed if seed is None else seed)
     bs, P = spec.bs, spec.page_size
     if spec.ragged is not None:
@@ -132,25 +157,21 @@ def make(spec: Spec, seed: Optional[int] = None, with_cache: bool = True) -> Wor
     q = torch.randn((bs, spec.num_q_heads, spec.head_dim), generator=g).to(torch.bfloat16)
     k_cache = v_cache = k_scale = v_scale = None
     if with_cache:
-        shape = (spec.num_pages, spec.num_kv_heads, P, spec.head_dim)
-        if spec.kv_dtype == "bf16":
-            k_cache = torch.randn(shape, generator=g).to(torch.bfloat16)
-            v_cache = torch.randn(shape, generator=g).to(torch.bfloat16)
-        elif spec.kv_dtype == "int8":
-            k_cache = torch.randint(-127, 128, shape, generator=g, dtype=torch.int8)
-            v_cache = torch.randint(-127, 128, shape, generator=g, dtype=torch.int8)
-            sshape = (spec.num_pages, spec.num_kv_heads, P)
-            k_scale = torch.rand(sshape, generator=g) * 0.045 + 0.005
-            v_scale = torch.rand(sshape, generator=g) * 0.045 + 0.005
-        else:
-            raise ValueError(spec.kv_dtype)
+        k_cache, v_cache, k_scale, v_scale = _draw_cache(spec, spec.num_pages, g)
 
     mapping = swa_pages = window_start = None
+    swa_num_pages = 0
     if spec.swa_window is not None:
-        mapping, swa_pages, window_start = _swa_mapping(spec, ctx, pages, g)
+        mapping, swa_pages, window_start, swa_num_pages = _swa_mapping(spec, ctx, pages, g)
 
-    return Workload(spec, ctx, pages, rpi, seq_lens, req_to_token, max_seq_pages, q,
-                    k_cache, v_cache, k_scale, v_scale, mapping, swa_pages, window_start)
+    wl = Workload(spec, ctx, pages, rpi, seq_lens, req_to_token, max_seq_pages, q,
+                  k_cache, v_cache, k_scale, v_scale, mapping, swa_pages, window_start,
+                  swa_num_pages)
+    if with_swa_cache:
+        if spec.swa_window is None:
+            raise ValueError(f"{spec.name}: no sliding window")
+        wl.k_swa, wl.v_swa, wl.k_swa_scale, wl.v_swa_scale = _draw_cache(spec, swa_num_pages, g)
+    return wl
 
 
 def _swa_mapping(spec: Spec, ctx, pages, g):
@@ -158,8 +179,11 @@ def _swa_mapping(spec: Spec, ctx, pages, g):
 
     For a request of length n, the window is token positions j >= n - window.  Every
     full-pool page that holds a window token gets its own page of a shuffled
-    sliding-window pool, and each window token's slot maps to the same offset in
-    that page.  Every other entry, and the extra page_size + 1 tail, is -1.
+    sliding-window pool, page for page: each slot of that page maps to the same offset
+    in its sliding-window page (the pool allocates whole pages, so the first slot of a
+    page the window starts inside is mapped too).  Every other entry, and the extra
+    page_size + 1 tail, is -1.  Returns (mapping, per-request {page: swa page},
+    per-request window start, sliding-window pool pages).
     """
     P, W = spec.page_size, spec.swa_window
     full_size = spec.num_pages * P
@@ -173,13 +197,12 @@ def _swa_mapping(spec: Spec, ctx, pages, g):
         for p in range(w0 // P, _cdiv(n, P)):
             assigned[p] = swa_perm[cursor]
             cursor += 1
+        offs = torch.arange(P, dtype=torch.int64)
         for p, sp in assigned.items():
-            lo, hi = max(p * P, w0), min((p + 1) * P, n)
-            offs = torch.arange(lo - p * P, hi - p * P, dtype=torch.int64)
             mapping[pg[p] * P + offs] = sp * P + offs
         swa_pages.append(assigned)
         window_start.append(w0)
-    return mapping, swa_pages, window_start
+    return mapping, swa_pages, window_start, swa_pool
 
 
 def draw_query_lengths(bs: int, max_q_len: int, seed: int) -> torch.Tensor:

@@ -141,15 +141,12 @@ def check_metadata_against_generator(wl, lib=None):
 
 
 def _swa_page_of_slot(wl, slot):
-    """Sliding-window page of a full-pool slot, from the generator's own record."""
+    """Sliding-window page of a full-pool slot, from the generator's own record (the
+    pool maps whole pages: every page holding a token of the window)."""
     P = wl.spec.page_size
     for r, pages in enumerate(wl.pages):
         if slot // P in pages:
-            p = pages.index(slot // P)
-            j = p * P + slot % P
-            if wl.swa_window_start[r] <= j < wl.ctx[r]:
-                return wl.swa_pages[r][p]
-            return -1
+            return wl.swa_pages[r].get(pages.index(slot // P), -1)
     return -1
 
 
@@ -369,6 +366,22 @@ PLANTS = {
 }
 
 
+def plant_source(src, before, after, function=None):
+    """``src`` with the first occurrence of ``before`` (after the start of ``function``
+    when given) replaced by ``after``; the occurrence must lie inside that function's
+    definition (before the next top-level ``int oracle_`` definition)."""
+    start = src.find(f"int {function}(") if function else 0
+    assert start >= 0, function
+    site = src.find(before, start)
+    assert site >= 0, before
+    head = src.rfind("\nint oracle_", 0, site)
+    nxt = src.find("\nint oracle_", head + 1)
+    assert nxt == -1 or site < nxt, before
+    if function:
+        assert src.rfind(f"\nint {function}(", 0, site) == head, (function, before)
+    return src[:site] + after + src[site + len(before):]
+
+
 def _run_all_pins(lib):
     check_metadata_hand_example(lib)
     check_negative_token_reading(lib)
@@ -396,13 +409,10 @@ def test_unplanted_build_passes_all_pins(tmp_path):
 def test_planted_mistakes_are_caught(plant, tmp_path):
     before, after = PLANTS[plant]
     src = open(oracle._SRC).read()
-    # the site is unique, or (for lines the multi-query function repeats) its first
-    # occurrence, in the decode function before it
-    first = src.find(before)
-    assert first >= 0 and (src.count(before) == 1 or
-                           first < src.find("int oracle_paged_attention_multi(")), plant
+    # the site is unique, or (for lines later functions repeat) its first occurrence,
+    # inside the first function that holds it
     path = tmp_path / f"{plant}.cpp"
-    path.write_text(src.replace(before, after, 1))
+    path.write_text(plant_source(src, before, after))
     lib = oracle.load(oracle.build(str(path), str(tmp_path / f"lib{plant}.so")))
     with pytest.raises(AssertionError):
         _run_all_pins(lib)
