@@ -208,6 +208,52 @@ PA_API pa_status pa_decode_splitk_multi(
     float* scratch_m, float* scratch_l, float* scratch_acc, void* stream, int32_t use_pdl);
 
 /*
+ * pa_decode_splitk_window -- the producer for sliding-window attention layers, reading
+ * the sliding-window pool through the sliding-window page table that the metadata
+ * module builds (sglang trtllm_mha_graph_metadata.py, module docstring: swa_page_table
+ * = full_to_swa_mapping[token] // page_size, -1 where the slot is unmapped).  The pages
+ * build that table but print no attention that reads it; this call is the plainest
+ * reading:
+ *   query i of request b (position pos = n - q_len + i, n = cache_seqlens[b]) attends the
+ *   positions j with max(0, pos - sliding_window + 1) <= j <= pos whose table entry
+ *   page_table[b, j / page_size] is >= 0; token j is row j % page_size of that page of
+ *   the pool (k_cache / v_cache / scales laid out as for pa_decode_splitk).  Pages with a
+ *   -1 entry are skipped: nothing is loaded from them and their tokens are not attended.
+ * Query rows: one per request (row b) when cu_seqlens_q is NULL, else as for
+ * pa_decode_splitk_multi (max_q_len queries at most per request).
+ * Split partition: the splits cover the window rather than the whole context.  With
+ * W = pa_window_pages(sliding_window, q_len_max, page_size, max_seq_pages) (q_len_max =
+ * max_q_len, or 1 without cu_seqlens_q) and L = page_size * ceil(W / num_splits), split
+ * s of request b holds positions [base + s L, base + (s+1) L), base = page_size *
+ * floor(max(0, n - q_len - sliding_window + 1) / page_size) (the page of the request's
+ * first visible position).  Scratch layouts and the empty-split convention are those of
+ * pa_decode_splitk(_multi); pa_reduce combines them.
+ * page_table here is the sliding-window table ([bs, page_table_stride] int32, entries
+ * -1 or in [0, num_pages)) and num_pages the sliding-window pool's page count.
+ * Errors: PA_ERR_INVALID for sliding_window < 1 and as pa_decode_splitk(_multi);
+ * PA_ERR_UNSUPPORTED when the CUDA-core producer is selected, when
+ * max_seq_pages * page_size > 2^29, or as pa_decode_splitk_multi for cu_seqlens_q.
+ */
+PA_API pa_status pa_decode_splitk_window(
+    const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+    const float* v_scale, int32_t kv_dtype, const int32_t* page_table, int64_t page_table_stride,
+    const int32_t* cache_seqlens, const int32_t* cu_seqlens_q, int32_t bs, int32_t max_q_len,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+    int64_t num_pages, int32_t max_seq_pages, int32_t sliding_window, int32_t num_splits,
+    float sm_scale, float* scratch_m, float* scratch_l, float* scratch_acc, void* stream,
+    int32_t use_pdl);
+
+/*
+ * Pages a sliding-window split partition spans: min(max_seq_pages,
+ * floor((sliding_window + max_q_len - 2) / page_size) + 2), the most pages that the
+ * sliding_window + max_q_len - 1 consecutive positions a request's queries can see may
+ * touch.  0 for a non-positive argument.  pa_choose_splits(bs, num_kv_heads, this,
+ * page_size, 0) is the split count pa_decode_step_window picks.
+ */
+PA_API int32_t pa_window_pages(int32_t sliding_window, int32_t max_q_len, int32_t page_size,
+                               int32_t max_seq_pages);
+
+/*
  * pa_reduce -- the log-sum-exp reducer (the standard and quantized reducer paths of
  * lmdeploy PR #4861 read the same fp32 partials, so one reducer serves both KV types):
  *   M = max_s m_s;  L = sum_s l_s exp(m_s - M)
@@ -243,6 +289,29 @@ PA_API pa_status pa_decode_step(
     int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t num_splits,
     float sm_scale, void* workspace, size_t workspace_bytes, void* out, float* lse,
     void* stream, int32_t use_pdl);
+
+/*
+ * pa_decode_step_window -- pa_decode_step for a sliding-window attention layer: the
+ * metadata stage (full_to_swa_mapping and swa_page_table are required here), then
+ * pa_decode_splitk_window over swa_page_table with one query per request, then
+ * pa_reduce.  k_swa / v_swa / the scales and num_swa_pages describe the sliding-window
+ * pool.  With num_splits == 0 the split count is
+ * pa_choose_splits(bs, num_kv_heads, pa_window_pages(sliding_window, 1, page_size,
+ * max_seq_pages), page_size, 0), and the workspace must hold
+ * pa_workspace_bytes(bs, num_q_heads, head_dim, that count).  Errors as the calls it makes.
+ */
+PA_API pa_status pa_decode_step_window(
+    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
+    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const void* q,
+    const void* k_swa, const void* v_swa, const float* k_swa_scale, const float* v_swa_scale,
+    int32_t kv_dtype, int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t page_size, int64_t num_swa_pages, int32_t sliding_window,
+    int32_t num_splits, float sm_scale, void* workspace, size_t workspace_bytes, void* out,
+    float* lse, void* stream, int32_t use_pdl);
 
 /*
  * pa_decode_step_static_scratch -- pa_decode_step for callers that cannot allocate

@@ -93,10 +93,18 @@ def _declare(lib):
     lib.pa_decode_splitk_multi.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, vp, i32, i32,
                                            i32, i32, i32, i32, i64, i32, i32, f32, vp, vp, vp,
                                            vp, i32]
+    lib.pa_decode_splitk_window.argtypes = [vp, vp, vp, vp, vp, i32, vp, i64, vp, vp, i32, i32,
+                                            i32, i32, i32, i32, i64, i32, i32, i32, f32, vp, vp,
+                                            vp, vp, i32]
+    lib.pa_window_pages.argtypes = [i32, i32, i32, i32]
+    lib.pa_window_pages.restype = i32
     lib.pa_reduce.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32]
     lib.pa_decode_step.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp, vp, vp, i64,
                                    vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                    i64, i32, f32, vp, sz, vp, vp, vp, i32]
+    lib.pa_decode_step_window.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp, vp, vp,
+                                          i64, vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                          i32, i32, i64, i32, i32, f32, vp, sz, vp, vp, vp, i32]
     lib.pa_decode_step_static_scratch.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp,
                                                   vp, vp, i64, vp, i64, vp, vp, vp, vp, vp, i32,
                                                   i32, i32, i32, i32, i32, i64, i32, f32, vp, vp,
@@ -114,8 +122,8 @@ def _declare(lib):
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_read_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     for name in ("pa_build_metadata", "pa_build_metadata_full", "pa_decode_splitk",
-                 "pa_decode_splitk_multi", "pa_reduce",
-                 "pa_decode_step", "pa_read_error_flags"):
+                 "pa_decode_splitk_multi", "pa_decode_splitk_window", "pa_reduce",
+                 "pa_decode_step", "pa_decode_step_window", "pa_read_error_flags"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -264,6 +272,38 @@ def pa_decode_splitk_multi(q, k_cache, v_cache, page_table, cache_seqlens, cu_se
     _check("pa_decode_splitk_multi", st)
 
 
+def pa_decode_splitk_window(q, k_cache, v_cache, page_table, cache_seqlens, scratch_m,
+                            scratch_l, scratch_acc, *, sliding_window: int, max_seq_pages: int,
+                            num_splits: int, sm_scale: float, cu_seqlens_q=None,
+                            max_q_len: int = 1, k_scale=None, v_scale=None, stream=None,
+                            use_pdl: bool = True):
+    """Split-K producer of a sliding-window layer: reads the sliding-window pool
+    (``k_cache``/``v_cache``) through the sliding-window page table; one query per
+    request, or the rows ``cu_seqlens_q`` assigns.  See include/pa.h."""
+    lib = load()
+    kv_dtype, ks, vs = _kv_args(k_cache, v_cache, k_scale, v_scale)
+    rows, hq, d = q.shape
+    bs = cache_seqlens.shape[0]
+    num_pages, hkv, page_size, _ = k_cache.shape
+    st = lib.pa_decode_splitk_window(
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
+        ks, vs, kv_dtype, _ptr2d(page_table, torch.int32, "page_table"),
+        _row_stride(page_table, "page_table"), _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
+        _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q"), bs, int(max_q_len), hq, hkv, d,
+        page_size, num_pages, int(max_seq_pages), int(sliding_window), int(num_splits),
+        float(sm_scale), _ptr(scratch_m, torch.float32, "scratch_m"),
+        _ptr(scratch_l, torch.float32, "scratch_l"), _ptr(scratch_acc, torch.float32, "scratch_acc"),
+        _stream(stream), int(bool(use_pdl)))
+    _check("pa_decode_splitk_window", st)
+
+
+def pa_window_pages(sliding_window: int, max_q_len: int, page_size: int,
+                    max_seq_pages: int) -> int:
+    """Pages a sliding-window split partition spans; see include/pa.h."""
+    return int(load().pa_window_pages(int(sliding_window), int(max_q_len), int(page_size),
+                                      int(max_seq_pages)))
+
+
 def pa_reduce(scratch_m, scratch_l, scratch_acc, out, lse=None, *, stream=None,
               use_pdl: bool = True):
     """Log-sum-exp reducer: writes out (bf16) and lse (fp32); see include/pa.h."""
@@ -306,6 +346,35 @@ def pa_decode_step(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: i
         workspace.numel() * workspace.element_size(), _ptr(out, torch.bfloat16, "out"),
         _ptr(lse, torch.float32, "lse"), _stream(stream), int(bool(use_pdl)))
     _check("pa_decode_step", st, lib)
+
+
+def pa_decode_step_window(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: int,
+                          max_seq_pages: int, cache_seqlens, cu_seqlens_k, page_table,
+                          full_to_swa_mapping, swa_page_table, q, k_swa, v_swa,
+                          sliding_window: int, num_splits: int, sm_scale: float, workspace,
+                          out, lse=None, k_swa_scale=None, v_swa_scale=None, stream=None,
+                          use_pdl: bool = True, lib=None):
+    """Metadata + sliding-window producer + reducer in one call; see include/pa.h."""
+    lib = lib or load()
+    kv_dtype, ks, vs = _kv_args(k_swa, v_swa, k_swa_scale, v_swa_scale)
+    bs, hq, d = q.shape
+    num_pages, hkv, page_size, _ = k_swa.shape
+    st = lib.pa_decode_step_window(
+        _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
+        _ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
+        req_to_token.shape[0], req_to_token.stride(0),
+        _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
+        full_to_swa_mapping.numel(), int(seqlen_offset), int(max_seq_pages),
+        _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
+        _ptr(cu_seqlens_k, torch.int32, "cu_seqlens_k"), _ptr2d(page_table, torch.int32, "page_table"),
+        _row_stride(page_table, "page_table"), _ptr2d(swa_page_table, torch.int32, "swa_page_table"),
+        _row_stride(swa_page_table, "swa_page_table"), _ptr(q, torch.bfloat16, "q"),
+        _ptr(k_swa, None, "k_swa"), _ptr(v_swa, None, "v_swa"), ks, vs, kv_dtype, bs, hq, hkv, d,
+        page_size, num_pages, int(sliding_window), int(num_splits), float(sm_scale),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream),
+        int(bool(use_pdl)))
+    _check("pa_decode_step_window", st, lib)
 
 
 def pa_decode_step_static_scratch(*, req_pool_indices, seq_lens, req_to_token,

@@ -224,9 +224,10 @@ pa_status decode_splitk_impl(const void* q, const void* k_cache, const void* v_c
                              const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
                              int32_t max_q_len, int32_t bs, int32_t num_q_heads,
                              int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
-                             int64_t num_pages, int32_t max_seq_pages, int32_t num_splits,
-                             float sm_scale, float* scratch_m, float* scratch_l,
-                             float* scratch_acc, void* stream, int32_t use_pdl) {
+                             int64_t num_pages, int32_t max_seq_pages, int32_t window,
+                             int32_t num_splits, float sm_scale, float* scratch_m,
+                             float* scratch_l, float* scratch_acc, void* stream,
+                             int32_t use_pdl) {
   pa_status st = check_attention(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
                                  page_table_stride, cache_seqlens, bs, num_q_heads,
                                  num_kv_heads, head_dim, page_size, num_pages, max_seq_pages,
@@ -241,6 +242,18 @@ pa_status decode_splitk_impl(const void* q, const void* k_cache, const void* v_c
     if (use_fma || static_cast<int64_t>(group) * max_q_len > 16) return PA_ERR_UNSUPPORTED;
   }
   if (use_fma && group > 8) return PA_ERR_UNSUPPORTED;
+  const int32_t q_rows = cu_seqlens_q != nullptr ? max_q_len : 1;
+  int32_t split_pages = max_seq_pages;  // pages the split partition spans
+  if (window != 0) {
+    if (window < 0) return PA_ERR_INVALID;
+    if (use_fma) return PA_ERR_UNSUPPORTED;
+    // keeps every window bound the kernel forms within int32
+    if (static_cast<int64_t>(max_seq_pages) * page_size > (int64_t{1} << 29))
+      return PA_ERR_UNSUPPORTED;
+    const int64_t longest = static_cast<int64_t>(max_seq_pages) * page_size + q_rows;
+    if (window > longest) window = static_cast<int32_t>(longest);  // same positions
+    split_pages = pa_window_pages(window, q_rows, page_size, max_seq_pages);
+  }
   pa::SplitKParams p = {};
   p.q = q;
   p.k_cache = k_cache;
@@ -254,11 +267,12 @@ pa_status decode_splitk_impl(const void* q, const void* k_cache, const void* v_c
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = num_kv_heads;
   p.max_seq_pages = max_seq_pages;
-  p.pages_per_split = static_cast<int32_t>(cdiv(max_seq_pages, num_splits));
+  p.pages_per_split = static_cast<int32_t>(cdiv(split_pages, num_splits));
+  p.window = window;
   p.num_splits = num_splits;
   p.q_scale = sm_scale * 1.4426950408889634f;  // log2(e): the kernel works in base 2
   p.cu_seqlens_q = cu_seqlens_q;
-  p.max_q_len = cu_seqlens_q != nullptr ? max_q_len : 1;
+  p.max_q_len = q_rows;
   p.m_out = scratch_m;
   p.l_out = scratch_l;
   p.acc_out = scratch_acc;
@@ -266,7 +280,11 @@ pa_status decode_splitk_impl(const void* q, const void* k_cache, const void* v_c
   cudaError_t e = error_word(&p.err);
   if (e != cudaSuccess) return from_cuda(e, "error word lookup");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (kv_dtype == PA_KV_INT8) {
+  if (window > 0) {
+    e = kv_dtype == PA_KV_INT8
+            ? pa::launch_splitk_mma_window_int8(p, bs, group, page_size, s, use_pdl != 0)
+            : pa::launch_splitk_mma_window_bf16(p, bs, group, page_size, s, use_pdl != 0);
+  } else if (kv_dtype == PA_KV_INT8) {
     e = use_fma ? pa::launch_splitk_int8(p, bs, group, page_size, s, use_pdl != 0)
                 : pa::launch_splitk_mma_int8(p, bs, group, page_size, s, use_pdl != 0);
   } else {
@@ -291,7 +309,7 @@ pa_status pa_decode_splitk(const void* q, const void* k_cache, const void* v_cac
                            float* scratch_acc, void* stream, int32_t use_pdl) {
   return decode_splitk_impl(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
                             page_table_stride, cache_seqlens, nullptr, 1, bs, num_q_heads,
-                            num_kv_heads, head_dim, page_size, num_pages, max_seq_pages,
+                            num_kv_heads, head_dim, page_size, num_pages, max_seq_pages, 0,
                             num_splits, sm_scale, scratch_m, scratch_l, scratch_acc, stream,
                             use_pdl);
 }
@@ -309,8 +327,34 @@ pa_status pa_decode_splitk_multi(const void* q, const void* k_cache, const void*
   return decode_splitk_impl(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
                             page_table_stride, cache_seqlens, cu_seqlens_q, max_q_len, bs,
                             num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
-                            max_seq_pages, num_splits, sm_scale, scratch_m, scratch_l,
+                            max_seq_pages, 0, num_splits, sm_scale, scratch_m, scratch_l,
                             scratch_acc, stream, use_pdl);
+}
+
+pa_status pa_decode_splitk_window(const void* q, const void* k_cache, const void* v_cache,
+                                  const float* k_scale, const float* v_scale, int32_t kv_dtype,
+                                  const int32_t* page_table, int64_t page_table_stride,
+                                  const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
+                                  int32_t bs, int32_t max_q_len, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                  int64_t num_pages, int32_t max_seq_pages,
+                                  int32_t sliding_window, int32_t num_splits, float sm_scale,
+                                  float* scratch_m, float* scratch_l, float* scratch_acc,
+                                  void* stream, int32_t use_pdl) {
+  if (sliding_window < 1) return PA_ERR_INVALID;
+  return decode_splitk_impl(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
+                            page_table_stride, cache_seqlens, cu_seqlens_q,
+                            cu_seqlens_q != nullptr ? max_q_len : 1, bs, num_q_heads,
+                            num_kv_heads, head_dim, page_size, num_pages, max_seq_pages,
+                            sliding_window, num_splits, sm_scale, scratch_m, scratch_l,
+                            scratch_acc, stream, use_pdl);
+}
+
+int32_t pa_window_pages(int32_t sliding_window, int32_t max_q_len, int32_t page_size,
+                        int32_t max_seq_pages) {
+  if (sliding_window < 1 || max_q_len < 1 || page_size < 1 || max_seq_pages < 1) return 0;
+  const int64_t pages = (static_cast<int64_t>(sliding_window) + max_q_len - 2) / page_size + 2;
+  return static_cast<int32_t>(pages < max_seq_pages ? pages : max_seq_pages);
 }
 
 pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const float* scratch_acc,
@@ -364,7 +408,13 @@ int32_t pa_choose_splits(int32_t bs, int32_t num_kv_heads, int32_t max_seq_pages
   return static_cast<int32_t>(cdiv(max_seq_pages, pages_per_split));
 }
 
-pa_status pa_decode_step(
+}  // extern "C"
+
+namespace {
+
+// Metadata, producer and reducer; window > 0 runs the sliding-window producer over
+// swa_page_table (k/v/scales/num_pages then describe the sliding-window pool).
+pa_status decode_step_impl(
     const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
     int64_t req_to_token_rows, int64_t req_to_token_stride,
     const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
@@ -373,23 +423,29 @@ pa_status pa_decode_step(
     int32_t* swa_page_table, int64_t swa_page_table_stride, const void* q,
     const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale,
     int32_t kv_dtype, int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
-    int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t num_splits,
+    int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t window, int32_t num_splits,
     float sm_scale, void* workspace, size_t workspace_bytes, void* out, float* lse,
     void* stream, int32_t use_pdl) {
   if (bs < 0) return PA_ERR_INVALID;
   if (bs == 0) return PA_OK;
   if (num_splits < 0) return PA_ERR_INVALID;
+  if (window > 0 && (full_to_swa_mapping == nullptr || swa_page_table == nullptr))
+    return PA_ERR_INVALID;
+  const int32_t split_pages =
+      window > 0 ? pa_window_pages(window, 1, page_size, max_seq_pages) : max_seq_pages;
   const int32_t splits =
       num_splits > 0 ? num_splits
-                     : pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, 0);
+                     : pa_choose_splits(bs, num_kv_heads, split_pages, page_size, 0);
   pa_status st = check_metadata(req_pool_indices, seq_lens, req_to_token, req_to_token_rows,
                                 req_to_token_stride, full_to_swa_mapping,
                                 full_to_swa_mapping_len, cache_seqlens, cu_seqlens_k,
                                 page_table, page_table_stride, swa_page_table,
                                 swa_page_table_stride, bs, max_seq_pages, page_size);
   if (st != PA_OK) return st;
-  st = check_attention(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
-                       page_table_stride, cache_seqlens, bs, num_q_heads, num_kv_heads,
+  const int32_t* attn_table = window > 0 ? swa_page_table : page_table;
+  const int64_t attn_stride = window > 0 ? swa_page_table_stride : page_table_stride;
+  st = check_attention(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, attn_table,
+                       attn_stride, cache_seqlens, bs, num_q_heads, num_kv_heads,
                        head_dim, page_size, num_pages, max_seq_pages, splits);
   if (st != PA_OK) return st;
   if (!out || !workspace || !aligned16(workspace)) return PA_ERR_INVALID;
@@ -407,12 +463,60 @@ pa_status pa_decode_step(
                          swa_page_table, swa_page_table_stride, bs, seqlen_offset,
                          max_seq_pages, page_size, stream, use_pdl);
   if (st != PA_OK) return st;
-  st = pa_decode_splitk(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
-                        page_table_stride, cache_seqlens, bs, num_q_heads, num_kv_heads,
-                        head_dim, page_size, num_pages, max_seq_pages, splits, sm_scale, m, l,
-                        acc, stream, use_pdl);
+  st = decode_splitk_impl(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, attn_table,
+                          attn_stride, cache_seqlens, nullptr, 1, bs, num_q_heads,
+                          num_kv_heads, head_dim, page_size, num_pages, max_seq_pages, window,
+                          splits, sm_scale, m, l, acc, stream, use_pdl);
   if (st != PA_OK) return st;
   return pa_reduce(m, l, acc, bs, num_q_heads, head_dim, splits, out, lse, stream, use_pdl);
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode_step(
+    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
+    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const void* q,
+    const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale,
+    int32_t kv_dtype, int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t num_splits,
+    float sm_scale, void* workspace, size_t workspace_bytes, void* out, float* lse,
+    void* stream, int32_t use_pdl) {
+  return decode_step_impl(req_pool_indices, seq_lens, req_to_token, req_to_token_rows,
+                          req_to_token_stride, full_to_swa_mapping, full_to_swa_mapping_len,
+                          seqlen_offset, max_seq_pages, cache_seqlens, cu_seqlens_k, page_table,
+                          page_table_stride, swa_page_table, swa_page_table_stride, q, k_cache,
+                          v_cache, k_scale, v_scale, kv_dtype, bs, num_q_heads, num_kv_heads,
+                          head_dim, page_size, num_pages, 0, num_splits, sm_scale, workspace,
+                          workspace_bytes, out, lse, stream, use_pdl);
+}
+
+pa_status pa_decode_step_window(
+    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
+    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const void* q,
+    const void* k_swa, const void* v_swa, const float* k_swa_scale, const float* v_swa_scale,
+    int32_t kv_dtype, int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t page_size, int64_t num_swa_pages, int32_t sliding_window,
+    int32_t num_splits, float sm_scale, void* workspace, size_t workspace_bytes, void* out,
+    float* lse, void* stream, int32_t use_pdl) {
+  if (sliding_window < 1) return PA_ERR_INVALID;
+  return decode_step_impl(req_pool_indices, seq_lens, req_to_token, req_to_token_rows,
+                          req_to_token_stride, full_to_swa_mapping, full_to_swa_mapping_len,
+                          seqlen_offset, max_seq_pages, cache_seqlens, cu_seqlens_k, page_table,
+                          page_table_stride, swa_page_table, swa_page_table_stride, q, k_swa,
+                          v_swa, k_swa_scale, v_swa_scale, kv_dtype, bs, num_q_heads,
+                          num_kv_heads, head_dim, page_size, num_swa_pages, sliding_window,
+                          num_splits, sm_scale, workspace, workspace_bytes, out, lse, stream,
+                          use_pdl);
 }
 
 #ifdef PA_TIMESTAMPS

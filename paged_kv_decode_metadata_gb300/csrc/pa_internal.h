@@ -58,6 +58,11 @@ struct SplitKParams {
   // one query per request (row b).
   const int32_t* cu_seqlens_q;
   int32_t max_q_len;
+  // Sliding window (tensor-core producer only): > 0 restricts query i of a request to
+  // its `window` newest positions, starts the split partition at the page of the
+  // request's first visible position, and skips pages whose table entry is -1.
+  // pages_per_split is then counted over the window's pages.  0: whole context.
+  int32_t window;
   float* m_out;
   float* l_out;
   float* acc_out;
@@ -95,6 +100,11 @@ cudaError_t launch_splitk_mma_bf16(const SplitKParams& p, int bs, int group, int
                                    cudaStream_t stream, bool use_pdl);
 cudaError_t launch_splitk_mma_int8(const SplitKParams& p, int bs, int group, int page_size,
                                    cudaStream_t stream, bool use_pdl);
+// Sliding-window variants (SplitKParams::window > 0).
+cudaError_t launch_splitk_mma_window_bf16(const SplitKParams& p, int bs, int group,
+                                          int page_size, cudaStream_t stream, bool use_pdl);
+cudaError_t launch_splitk_mma_window_int8(const SplitKParams& p, int bs, int group,
+                                          int page_size, cudaStream_t stream, bool use_pdl);
 
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool use_pdl);
 

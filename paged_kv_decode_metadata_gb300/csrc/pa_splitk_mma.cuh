@@ -42,6 +42,7 @@
 #include <math_constants.h>
 
 #include <atomic>
+#include <climits>
 #include <utility>
 
 #include "pa_common.cuh"
@@ -72,7 +73,8 @@ struct Layout {
   static constexpr int OFF_EMPTY = OFF_FULL + STAGES * 8;
   static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;      // [4 warps][16 columns][3]
   static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 3 * 4;    // abort flag
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;                         // + alignment slack
+  static constexpr int OFF_SKIP = OFF_MISC + 16;  // per stage: mask of its skipped pages
+  static constexpr int SMEM = OFF_SKIP + (STAGES * 4 + 15) / 16 * 16 + 1024;  // + alignment slack
   static constexpr int RED_BYTES = kConsumerWarps * 16 * 128 * 4;           // output merge buffer
   static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "merge buffer reuses the ring");
 };
@@ -220,7 +222,9 @@ __device__ __forceinline__ int64_t column_slot(int q_begin, int col, int G, int 
          split;
 }
 
-template <bool kQuant, int P, int STAGES, int MINB, int kNT>
+// kWindow: the sliding-window variant (prm.window > 0); without it every window test
+// folds away at compile time.
+template <bool kQuant, int P, int STAGES, int MINB, int kNT, bool kWindow>
 __global__ void __launch_bounds__(kThreads, MINB)
     splitk_mma_kernel(const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const SplitKParams prm) {
@@ -244,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   int32_t* pages_s = reinterpret_cast<int32_t*>(smem + L::OFF_PAGES);
   float* ml_s = reinterpret_cast<float*>(smem + L::OFF_ML);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC);
+  uint32_t* skip_s = reinterpret_cast<uint32_t*>(smem + L::OFF_SKIP);
 
   // ---- prologue independent of the metadata stage: Q^T fragments in registers ------
   // (with several queries per request their rows come from cu_seqlens_q, a metadata
@@ -279,18 +284,29 @@ __global__ void __launch_bounds__(kThreads, MINB)
   }
   const int ncols = q_len * G;  // (query, head) columns of this request and kv head
 
-  // The split's page indices and the request length are independent loads: issue both
-  // before either is used (page indices are bounds-checked where they are used).
-  const int p_begin = split * prm.pages_per_split;
-  const int32_t* pt_row =
-      prm.page_table + static_cast<int64_t>(b) * prm.page_table_stride + p_begin;
-  const int pages_cap = min(min(prm.pages_per_split, prm.max_seq_pages - p_begin), kMaxSplitPages);
-  for (int i = tid; i < pages_cap; i += kThreads) pages_s[i] = pt_row[i];
+  // Without a window the split's page indices and the request length are independent
+  // loads: issue both before either is used (page indices are bounds-checked where they
+  // are used).  With a window the split starts at the page of the request's first
+  // visible position, which depends on the length.
+  const int window = kWindow ? prm.window : 0;
+  int p_begin = split * prm.pages_per_split;
+  const int32_t* pt_row = prm.page_table + static_cast<int64_t>(b) * prm.page_table_stride;
+  auto cache_page_indices = [&]() {
+    pt_row += p_begin;
+    const int pages_cap =
+        min(min(prm.pages_per_split, prm.max_seq_pages - p_begin), kMaxSplitPages);
+    for (int i = tid; i < pages_cap; i += kThreads) pages_s[i] = pt_row[i];
+  };
+  if (window == 0) cache_page_indices();
   int n = prm.cache_seqlens[b];
   const int cap = prm.max_seq_pages * P;
   if (n < 0 || n > cap) {
     if (tid == 0 && split == 0 && kvh == 0) record_error(prm.err, kErrSeqLenOutOfRange);
     n = n < 0 ? 0 : cap;
+  }
+  if (window > 0) {
+    p_begin += max(0, n - q_len - window + 1) / P;
+    cache_page_indices();
   }
   const int n_pages = (n + P - 1) / P;
   const int p_end = min(p_begin + prm.pages_per_split, n_pages);
@@ -330,8 +346,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const uint32_t kdst = smem_base + stage * L::STAGE_BYTES;
         const uint32_t vdst = kdst + L::KV_BYTES;
         const int ctok = c * kChunk;
+        // -1: a page the sliding-window pool does not hold (window mode only); its
+        // tokens are skipped and nothing is loaded for it
         auto page_at = [&](int i) -> int {
           int32_t pg = i < kMaxSplitPages ? pages_s[i] : pt_row[i];
+          if (pg < 0 && window > 0) return -1;
           if (pg < 0 || pg >= prm.num_pages) {
             record_error(prm.err, kErrPageOutOfRange);
             pg = 0;
@@ -341,6 +360,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if constexpr (P >= kChunk) {
           const int pg = page_at(ctok / P);
           const int row = ctok % P;
+          // the mask is published by the arrive below (release) and read after the
+          // consumers' wait on the same barrier (acquire)
+          if constexpr (kWindow) {
+            skip_s[stage] = pg < 0 ? 1u : 0u;
+            if (pg < 0) {
+              mbar_arrive(&full[stage]);
+              continue;
+            }
+          }
           mbar_arrive_expect_tx(&full[stage], 2 * L::KV_BYTES + 2 * L::SCALE_BYTES);
           if constexpr (kQuant) {
             tma_load_4d(kdst, &map_k, 0, row, kvh, pg, &full[stage], policy);
@@ -363,10 +391,26 @@ __global__ void __launch_bounds__(kThreads, MINB)
           const int first = ctok / P;
           const int np = min(kPages, n_split_pages - first);
           constexpr int kPageRows = P * 128;  // bytes of one page's rows in a 128-B-row tile
+          int pgs[kPages];
+          uint32_t skip = 0;
+          int loaded = 0;
+#pragma unroll
+          for (int k = 0; k < kPages; ++k) {
+            pgs[k] = k < np ? page_at(first + k) : -1;
+            if (k < np && pgs[k] < 0) skip |= 1u << k;
+            loaded += pgs[k] >= 0 ? 1 : 0;
+          }
+          if constexpr (kWindow) skip_s[stage] = skip;
+          if (loaded == 0) {
+            mbar_arrive(&full[stage]);
+            continue;
+          }
           mbar_arrive_expect_tx(&full[stage],
-                                np * (kQuant ? 2 * (P * 128 + P * 4) : 2 * P * 256));
-          for (int k = 0; k < np; ++k) {
-            const int pg = page_at(first + k);
+                                loaded * (kQuant ? 2 * (P * 128 + P * 4) : 2 * P * 256));
+#pragma unroll
+          for (int k = 0; k < kPages; ++k) {
+            const int pg = pgs[k];
+            if (pg < 0) continue;
             if constexpr (kQuant) {
               tma_load_4d(kdst + k * kPageRows, &map_k, 0, 0, kvh, pg, &full[stage], policy);
               tma_load_4d(vdst + k * kPageRows, &map_v, 0, 0, kvh, pg, &full[stage], policy);
@@ -424,6 +468,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const int col = 8 * nt + 2 * tig + e;
       lim[nt][e] = col < ncols ? n - q_len + col / G + 1 - tok_begin : 0;
     }
+  // With a window, a column sees positions >= lim - window (its query's `window` newest
+  // positions); the largest such bound over the request's columns (its newest query,
+  // lim = n - tok_begin), relative to the split.
+  const int lo_hi = window > 0 ? n - window - tok_begin : INT_MIN;
 
   for (int c = 0; c < n_chunks; ++c) {
     const int stage = c % STAGES;
@@ -440,8 +488,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const uint32_t kst = smem_base + stage * L::STAGE_BYTES;
     const uint32_t vst = kst + L::KV_BYTES;
     const bool partial = valid < t0 + 16;
+    // a warp's 16 tokens lie on one page (P >= 16); a skipped page was not loaded
+    const bool skipped = window > 0 && ((skip_s[stage] >> (t0 / P)) & 1u);
+    const bool active = t0 < valid && !skipped;
+    // positions below a column's window start occur only in the first slices
+    const bool check_lo = c * kChunk + t0 < lo_hi;
 
-    if (t0 < valid) {
+    if (active) {
       // Rows of this warp's slice past the context: their V bytes are not ours to trust
       // (stale ring contents or cache slots past the request), so zero them before PV.
       if (partial) {
@@ -519,7 +572,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
           v *= q_scale;
           if constexpr (kQuant) v *= (i < 2 ? ks_a : ks_b);
           const int pos = c * kChunk + (i < 2 ? tok_a : tok_b);  // position in the split
-          x[i] = ((i < 2 ? tok_a : tok_b) < valid && pos < lim[nt][i & 1]) ? v : -CUDART_INF_F;
+          bool seen = (i < 2 ? tok_a : tok_b) < valid && pos < lim[nt][i & 1];
+          if (check_lo) seen = seen && pos >= lim[nt][i & 1] - window;
+          x[i] = seen ? v : -CUDART_INF_F;
         }
         // Reference maximum per column, moved only when a score exceeds it by more than
         // 2^kMaxSlack (one vote instead of a shuffle reduction and a rescale per slice);
@@ -618,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
     // this warp is done with the stage; zeroing stores (generic proxy) must be ordered
     // before the TMA (async proxy) refills the buffer
-    if (t0 < valid && partial) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (active && partial) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
   }
@@ -760,12 +815,12 @@ inline cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, bool quan
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool kQuant, int P, int STAGES, int MINB, int kNT>
+template <bool kQuant, int P, int STAGES, int MINB, int kNT, bool kWindow>
 cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
                            dim3 grid, cudaStream_t stream, bool use_pdl) {
   using L = Layout<kQuant, STAGES>;
   void (*kernel)(const CUtensorMap, const CUtensorMap, const SplitKParams) =
-      splitk_mma_kernel<kQuant, P, STAGES, MINB, kNT>;
+      splitk_mma_kernel<kQuant, P, STAGES, MINB, kNT, kWindow>;
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -783,7 +838,7 @@ cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const C
 
 // (STAGES, MINB) for G <= 8 (one n-tile of heads) and for G = 16 (two n-tiles, more
 // registers per thread).
-template <bool kQuant, int STAGES1, int MINB1, int STAGES2, int MINB2>
+template <bool kQuant, int STAGES1, int MINB1, int STAGES2, int MINB2, bool kWindow>
 cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_size,
                             cudaStream_t stream, bool use_pdl) {
   CUtensorMap mk, mv;
@@ -797,8 +852,10 @@ cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_s
 #define PA_MMA_CASE(PP)                                                                        \
   if (page_size == PP) {                                                                       \
     return two_tiles                                                                           \
-               ? launch_mma_one<kQuant, PP, STAGES2, MINB2, 2>(p, mk, mv, grid, stream, use_pdl) \
-               : launch_mma_one<kQuant, PP, STAGES1, MINB1, 1>(p, mk, mv, grid, stream, use_pdl); \
+               ? launch_mma_one<kQuant, PP, STAGES2, MINB2, 2, kWindow>(p, mk, mv, grid, stream,  \
+                                                                         use_pdl)               \
+               : launch_mma_one<kQuant, PP, STAGES1, MINB1, 1, kWindow>(p, mk, mv, grid, stream,  \
+                                                                         use_pdl);              \
   }
   PA_MMA_CASE(16)
   PA_MMA_CASE(32)

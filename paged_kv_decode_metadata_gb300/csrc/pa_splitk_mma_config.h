@@ -1,0 +1,34 @@
+// Pipeline depth (STAGES) and resident CTAs per SM (MINB) of the tensor-core split-K
+// producer, per KV type; suffix 1: G <= 8 query heads per KV head (one n-tile of
+// columns), suffix 2: up to 16 columns (two n-tiles, twice the output fragments).
+#pragma once
+
+// G <= 8: two 32 KiB stages (K + V of a 64-token chunk) per CTA, three CTAs per SM.
+// G = 16: three stages, two CTAs per SM (twice the output fragments per thread).
+#ifndef PA_MMA_BF16_STAGES1
+#define PA_MMA_BF16_STAGES1 2
+#endif
+#ifndef PA_MMA_BF16_MINB1
+#define PA_MMA_BF16_MINB1 3
+#endif
+#ifndef PA_MMA_BF16_STAGES2
+#define PA_MMA_BF16_STAGES2 3
+#endif
+#ifndef PA_MMA_BF16_MINB2
+#define PA_MMA_BF16_MINB2 2
+#endif
+
+// G <= 8: four 17 KiB stages (codes and scales of a 64-token chunk) per CTA, three CTAs
+// per SM.  G = 16: six stages, two CTAs per SM.
+#ifndef PA_MMA_INT8_STAGES1
+#define PA_MMA_INT8_STAGES1 4
+#endif
+#ifndef PA_MMA_INT8_MINB1
+#define PA_MMA_INT8_MINB1 3
+#endif
+#ifndef PA_MMA_INT8_STAGES2
+#define PA_MMA_INT8_STAGES2 6
+#endif
+#ifndef PA_MMA_INT8_MINB2
+#define PA_MMA_INT8_MINB2 2
+#endif

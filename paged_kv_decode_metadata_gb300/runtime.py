@@ -2,7 +2,9 @@
 
 ``DeviceStep`` holds device copies of a workload's inputs, the metadata outputs, the
 split-K scratch and the outputs, and runs the three stages through the C ABI, either
-one by one or as ``pa_decode_step``.
+one by one or as ``pa_decode_step``.  ``WindowStep`` adds the sliding-window pool of a
+workload drawn with one and runs the sliding-window layer's step
+(``pa_decode_step_window``).
 """
 
 from __future__ import annotations
@@ -29,8 +31,9 @@ class DeviceStep:
         self.seq_lens = wl.seq_lens.to(**to)
         self.req_to_token = wl.req_to_token.to(**to)
         self.q = wl.q.to(**to)
-        self.k_cache = wl.k_cache.to(**to)
-        self.v_cache = wl.v_cache.to(**to)
+        # (a workload drawn without its full pool leaves these None)
+        self.k_cache = wl.k_cache.to(**to) if wl.k_cache is not None else None
+        self.v_cache = wl.v_cache.to(**to) if wl.v_cache is not None else None
         self.k_scale = wl.k_scale.to(**to) if wl.k_scale is not None else None
         self.v_scale = wl.v_scale.to(**to) if wl.v_scale is not None else None
         self.full_to_swa_mapping = (wl.full_to_swa_mapping.to(**to)
@@ -113,3 +116,53 @@ class DeviceStep:
         if self.swa_page_table is not None:
             meta += self.bs * self.max_seq_pages * (4 + 8)
         return self.kv_bytes(ctx) + q_o + scratch + meta
+
+
+class WindowStep(DeviceStep):
+    """A sliding-window layer's decode step: the metadata stage, then the window
+    producer over ``swa_page_table`` and the sliding-window pool, then the reducer."""
+
+    def __init__(self, wl, device="cuda", num_splits: int | None = None):
+        if wl.k_swa is None:
+            raise ValueError("workload drawn without a sliding-window pool")
+        spec = wl.spec
+        self.window = int(spec.swa_window)
+        if num_splits is None:
+            pages = B.pa_window_pages(self.window, 1, spec.page_size, wl.max_seq_pages)
+            num_splits = B.pa_choose_splits(spec.bs, spec.num_kv_heads, pages, spec.page_size)
+        super().__init__(wl, device=device, num_splits=num_splits, with_swa=True)
+        to = dict(device=device)
+        # the full pool is not read by this step: the sliding-window pool takes its place
+        self.k_cache = wl.k_swa.to(**to)
+        self.v_cache = wl.v_swa.to(**to)
+        self.k_scale = wl.k_swa_scale.to(**to) if wl.k_swa_scale is not None else None
+        self.v_scale = wl.v_swa_scale.to(**to) if wl.v_swa_scale is not None else None
+
+    def splitk(self, use_pdl=True, stream=None):
+        B.pa_decode_splitk_window(self.q, self.k_cache, self.v_cache, self.swa_page_table,
+                                  self.cache_seqlens, self.scratch_m, self.scratch_l,
+                                  self.scratch_acc, sliding_window=self.window,
+                                  max_seq_pages=self.max_seq_pages, num_splits=self.num_splits,
+                                  sm_scale=self.sm_scale, k_scale=self.k_scale,
+                                  v_scale=self.v_scale, stream=stream, use_pdl=use_pdl)
+
+    def step(self, use_pdl=True, stream=None, lib=None):
+        B.pa_decode_step_window(req_pool_indices=self.req_pool_indices, seq_lens=self.seq_lens,
+                                req_to_token=self.req_to_token, seqlen_offset=self.seqlen_offset,
+                                max_seq_pages=self.max_seq_pages, cache_seqlens=self.cache_seqlens,
+                                cu_seqlens_k=self.cu_seqlens_k, page_table=self.page_table,
+                                full_to_swa_mapping=self.full_to_swa_mapping,
+                                swa_page_table=self.swa_page_table, q=self.q, k_swa=self.k_cache,
+                                v_swa=self.v_cache, sliding_window=self.window,
+                                num_splits=self.num_splits, sm_scale=self.sm_scale,
+                                workspace=self.workspace, out=self.out, lse=self.lse,
+                                k_swa_scale=self.k_scale, v_swa_scale=self.v_scale,
+                                stream=stream, use_pdl=use_pdl, lib=lib)
+
+    def visible_tokens(self, ctx) -> list:
+        """Positions each request's query attends: min(n, window)."""
+        return [min(int(n), self.window) for n in ctx]
+
+    def kv_bytes(self, ctx) -> int:
+        """Bytes of K and V (plus int8 scales) the step must read: the window's tokens."""
+        return super().kv_bytes(self.visible_tokens(ctx))

@@ -122,8 +122,9 @@ def _draw_cache(spec: Spec, num_pages: int, g: torch.Generator):
 def make(spec: Spec, seed: Optional[int] = None, with_cache: bool = True,
          with_swa_cache: bool = False) -> Workload:
     """Draw one workload.  ``with_cache=False`` skips the (large) K/V pools;
-    ``with_swa_cache`` also draws the sliding-window pool (after everything else, so
-    the other tensors do not depend on it)."""
+    ``with_swa_cache`` also draws the sliding-window pool, from a generator of its own
+    (seed + 0x5A5A), so neither it nor the other tensors depend on which pools are
+    drawn."""
     g = torch.Generator().manual_seed(spec.seed if seed is None else seed)
     bs, P = spec.bs, spec.page_size
     if spec.ragged is not None:
@@ -170,7 +171,9 @@ def make(spec: Spec, seed: Optional[int] = None, with_cache: bool = True,
     if with_swa_cache:
         if spec.swa_window is None:
             raise ValueError(f"{spec.name}: no sliding window")
-        wl.k_swa, wl.v_swa, wl.k_swa_scale, wl.v_swa_scale = _draw_cache(spec, swa_num_pages, g)
+        g_swa = torch.Generator().manual_seed((spec.seed if seed is None else seed) + 0x5A5A)
+        wl.k_swa, wl.v_swa, wl.k_swa_scale, wl.v_swa_scale = _draw_cache(spec, swa_num_pages,
+                                                                         g_swa)
     return wl
 
 
