@@ -43,6 +43,8 @@ def parse():
                     help="skip the PDL study, e2e and CPU baseline")
     ap.add_argument("--profile", action="store_true",
                     help="eager steps only (warm-up + steps launches of each kernel), for ncu")
+    ap.add_argument("--window", action="store_true",
+                    help="with --profile: the workload's sliding-window layer step instead")
     ap.add_argument("--all-workloads", action="store_true",
                     help="report table: every named workload, graph with / without PDL and "
                          "eager (one JSON line per workload; not the benchmark line)")
@@ -60,8 +62,9 @@ def measured_peaks():
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_metadata_gb300", "csrc")
-    for name in ("pa_splitk_mma.cuh", "pa_common.cuh", "pa_splitk_mma_bf16.cu",
-                 "pa_splitk_mma_int8.cu"):
+    for name in ("pa_splitk_mma.cuh", "pa_common.cuh", "pa_splitk_mma_config.h",
+                 "pa_splitk_mma_bf16.cu", "pa_splitk_mma_int8.cu",
+                 "pa_splitk_mma_window_bf16.cu", "pa_splitk_mma_window_int8.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -504,11 +507,24 @@ def run_table(args):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     stream = torch.cuda.Stream()
     l2_bytes = torch.cuda.get_device_properties(0).L2_cache_size
+    from paged_kv_decode_metadata_gb300.runtime import WindowStep
+
     per_graph = 8
-    for name in synthetic.WORKLOAD_ORDER:
-        wl = synthetic.make(synthetic.WORKLOADS[name])
-        ds = DeviceStep(wl)
-        row = {"workload": name, "num_splits": ds.num_splits, "steps_per_graph": per_graph}
+    # every named workload, then the sliding-window layer of the ones that have a window
+    rows = [(n, False) for n in synthetic.WORKLOAD_ORDER]
+    rows += [(n, True) for n in synthetic.WORKLOAD_ORDER
+             if synthetic.WORKLOADS[n].swa_window is not None]
+    for name, window in rows:
+        spec = synthetic.WORKLOADS[name]
+        if window:
+            wl = synthetic.make(spec, with_cache=False, with_swa_cache=True)
+            make_step = lambda: WindowStep(wl)  # noqa: E731
+        else:
+            wl = synthetic.make(spec)
+            make_step = lambda: DeviceStep(wl)  # noqa: E731
+        ds = make_step()
+        row = {"workload": name + (f" window {spec.swa_window}" if window else ""),
+               "num_splits": ds.num_splits, "steps_per_graph": per_graph}
         reps = max(20, min(args.steps, 2000) // per_graph)
         for pdl in (False, True):
             def steps(pdl=pdl):
@@ -533,7 +549,7 @@ def run_table(args):
         footprint = ds.step_bytes(wl.ctx)
         if footprint < 2 * l2_bytes:
             copies = int(2 * l2_bytes // footprint) + 1
-            others = [DeviceStep(wl) for _ in range(copies - 1)]
+            others = [make_step() for _ in range(copies - 1)]
             everyone = [ds] + others
 
             def rotate():
@@ -568,16 +584,21 @@ def run_profile(args, spec):
 
     pa_build.build()
     binding.load()
-    wl = synthetic.make(spec)
-    ds = DeviceStep(wl)
+    if args.window:
+        from paged_kv_decode_metadata_gb300.runtime import WindowStep
+        wl = synthetic.make(spec, with_cache=False, with_swa_cache=True)
+        ds = WindowStep(wl)
+    else:
+        wl = synthetic.make(spec)
+        ds = DeviceStep(wl)
     for _ in range(args.warmup + args.steps):
         ds.step(use_pdl=True)
     torch.cuda.synchronize()
     flags = binding.pa_read_error_flags(reset=True)
     if flags:
         raise RuntimeError(f"device error flags 0x{flags:x}")
-    print(json.dumps({"profile": spec.name, "steps": args.warmup + args.steps,
-                      "num_splits": ds.num_splits}))
+    print(json.dumps({"profile": spec.name + (" window" if args.window else ""),
+                      "steps": args.warmup + args.steps, "num_splits": ds.num_splits}))
 
 
 def main():

@@ -248,7 +248,7 @@ PA_API pa_status pa_decode_splitk_window(
  * floor((sliding_window + max_q_len - 2) / page_size) + 2), the most pages that the
  * sliding_window + max_q_len - 1 consecutive positions a request's queries can see may
  * touch.  0 for a non-positive argument.  pa_choose_splits(bs, num_kv_heads, this,
- * page_size, 0) is the split count pa_decode_step_window picks.
+ * page_size, kv_dtype, 0) is the split count pa_decode_step_window picks.
  */
 PA_API int32_t pa_window_pages(int32_t sliding_window, int32_t max_q_len, int32_t page_size,
                                int32_t max_seq_pages);
@@ -274,7 +274,7 @@ PA_API pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const
  * too, and it waits before writing anything).  Arguments are those of the three
  * functions above.  The split-K scratch is carved from `workspace`
  * (workspace_bytes >= pa_workspace_bytes(bs, num_q_heads, head_dim, S)), where S is
- * num_splits, or pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, 0)
+ * num_splits, or pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, kv_dtype, 0)
  * when num_splits == 0.
  */
 PA_API pa_status pa_decode_step(
@@ -297,7 +297,7 @@ PA_API pa_status pa_decode_step(
  * pa_reduce.  k_swa / v_swa / the scales and num_swa_pages describe the sliding-window
  * pool.  With num_splits == 0 the split count is
  * pa_choose_splits(bs, num_kv_heads, pa_window_pages(sliding_window, 1, page_size,
- * max_seq_pages), page_size, 0), and the workspace must hold
+ * max_seq_pages), page_size, kv_dtype, 0), and the workspace must hold
  * pa_workspace_bytes(bs, num_q_heads, head_dim, that count).  Errors as the calls it makes.
  */
 PA_API pa_status pa_decode_step_window(
@@ -354,13 +354,17 @@ PA_API size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_d
                           int32_t num_splits);
 
 /*
- * Split count heuristic: enough (request, kv head, split) blocks for several waves
- * of the GPU's SMs, a page-aligned split length, and no split count that leaves the
- * longest request with an empty split.  sm_count <= 0 queries the current device.
- * Returns >= 1 (1 for degenerate sizes).
+ * Split count heuristic, measured on GB300: a split holds about 2048 positions of the
+ * longest request for bf16 KV and 4096 for int8 KV (whose producer spends more time
+ * per block outside the KV stream), but there are at least 2.5 waves of
+ * (request, kv head, split) blocks at three resident blocks per SM; each split holds at
+ * least two 64-token chunks, its length is page-aligned, and no split count leaves the
+ * longest request with an empty split.  kv_dtype is PA_KV_BF16 or PA_KV_INT8 (any other
+ * value is read as bf16); sm_count <= 0 queries the current device.  Returns >= 1
+ * (1 for degenerate sizes).
  */
 PA_API int32_t pa_choose_splits(int32_t bs, int32_t num_kv_heads, int32_t max_seq_pages,
-                         int32_t page_size, int32_t sm_count);
+                                int32_t page_size, int32_t kv_dtype, int32_t sm_count);
 
 /*
  * Choose the split-K producer implementation for later calls in this process

@@ -112,7 +112,7 @@ def _declare(lib):
     lib.pa_decode_step_static_scratch.restype = ctypes.c_int
     lib.pa_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.pa_workspace_bytes.restype = sz
-    lib.pa_choose_splits.argtypes = [i32, i32, i32, i32, i32]
+    lib.pa_choose_splits.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.pa_choose_splits.restype = i32
     lib.pa_select_producer.argtypes = [i32]
     lib.pa_select_producer.restype = i32
@@ -413,8 +413,10 @@ def pa_workspace_bytes(bs: int, num_q_heads: int, head_dim: int, num_splits: int
 
 
 def pa_choose_splits(bs: int, num_kv_heads: int, max_seq_pages: int, page_size: int,
-                     sm_count: int = 0) -> int:
-    return int(load().pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, sm_count))
+                     kv_dtype: int = 0, sm_count: int = 0) -> int:
+    """Split count heuristic; kv_dtype PA_KV_BF16 (0) or PA_KV_INT8 (1)."""
+    return int(load().pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, kv_dtype,
+                                       sm_count))
 
 
 def pa_select_producer(producer: int) -> int:

@@ -388,17 +388,22 @@ size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim,
 }
 
 int32_t pa_choose_splits(int32_t bs, int32_t num_kv_heads, int32_t max_seq_pages,
-                         int32_t page_size, int32_t sm_count) {
+                         int32_t page_size, int32_t kv_dtype, int32_t sm_count) {
   if (bs <= 0 || num_kv_heads <= 0 || max_seq_pages <= 0 || page_size <= 0) return 1;
   if (sm_count <= 0) sm_count = sm_count_of_current_device();
   if (sm_count <= 0) sm_count = 152;
-  // Aim for about eight waves of two resident blocks per SM, so the block scheduler
-  // can balance ragged requests and the last wave is a small fraction of the step.
+  // Positions of the longest request per split: the int8 producer's per-block work
+  // outside the KV stream (Q conversion, merge) favours longer splits (GB300 sweeps:
+  // best near 2048 for bf16, 4096 for int8, on uniform and ragged batches).
+  const int64_t tokens = static_cast<int64_t>(max_seq_pages) * page_size;
+  int64_t want = cdiv(tokens, kv_dtype == PA_KV_INT8 ? 4096 : 2048);
+  // ... but at least 2.5 waves of blocks at three resident blocks per SM, so the
+  // scheduler can balance ragged requests and the last wave is not most of the step.
   const int64_t units = static_cast<int64_t>(bs) * num_kv_heads;
-  const int64_t target_blocks = static_cast<int64_t>(sm_count) * 2 * 8;
-  int64_t want = cdiv(target_blocks, units);
+  const int64_t waves = cdiv(static_cast<int64_t>(sm_count) * 3 * 5, 2 * units);
+  if (want < waves) want = waves;
   // At least two 64-token chunks per split keep the per-block prologue amortised.
-  const int64_t chunks = cdiv(static_cast<int64_t>(max_seq_pages) * page_size, 64);
+  const int64_t chunks = cdiv(tokens, 64);
   const int64_t most = chunks / 2 > 0 ? chunks / 2 : 1;
   if (want > most) want = most;
   if (want < 1) want = 1;
@@ -435,7 +440,7 @@ pa_status decode_step_impl(
       window > 0 ? pa_window_pages(window, 1, page_size, max_seq_pages) : max_seq_pages;
   const int32_t splits =
       num_splits > 0 ? num_splits
-                     : pa_choose_splits(bs, num_kv_heads, split_pages, page_size, 0);
+                     : pa_choose_splits(bs, num_kv_heads, split_pages, page_size, kv_dtype, 0);
   pa_status st = check_metadata(req_pool_indices, seq_lens, req_to_token, req_to_token_rows,
                                 req_to_token_stride, full_to_swa_mapping,
                                 full_to_swa_mapping_len, cache_seqlens, cu_seqlens_k,

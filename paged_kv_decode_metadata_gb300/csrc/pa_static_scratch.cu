@@ -69,7 +69,8 @@ extern "C" pa_status pa_decode_step_static_scratch(
   if (bs == 0) return PA_OK;
   const int32_t splits =
       num_splits > 0 ? num_splits
-                     : pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, 0);
+                     : pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, kv_dtype,
+                                        0);
   const size_t need = pa_workspace_bytes(bs, num_q_heads, head_dim, splits);
   if (need == 0) return PA_ERR_INVALID;
   if (need > PA_STATIC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;

@@ -39,8 +39,9 @@ class DeviceStep:
         self.full_to_swa_mapping = (wl.full_to_swa_mapping.to(**to)
                                     if with_swa and wl.full_to_swa_mapping is not None else None)
         if num_splits is None:
+            kv = B.PA_KV_INT8 if spec.kv_dtype == "int8" else B.PA_KV_BF16
             num_splits = spec.num_splits or B.pa_choose_splits(
-                self.bs, self.num_kv_heads, self.max_seq_pages, self.page_size)
+                self.bs, self.num_kv_heads, self.max_seq_pages, self.page_size, kv)
         self.num_splits = int(num_splits)
         pts = page_table_stride or self.max_seq_pages
         i32 = dict(dtype=torch.int32, device=device)
@@ -129,7 +130,8 @@ class WindowStep(DeviceStep):
         self.window = int(spec.swa_window)
         if num_splits is None:
             pages = B.pa_window_pages(self.window, 1, spec.page_size, wl.max_seq_pages)
-            num_splits = B.pa_choose_splits(spec.bs, spec.num_kv_heads, pages, spec.page_size)
+            kv = B.PA_KV_INT8 if spec.kv_dtype == "int8" else B.PA_KV_BF16
+            num_splits = B.pa_choose_splits(spec.bs, spec.num_kv_heads, pages, spec.page_size, kv)
         super().__init__(wl, device=device, num_splits=num_splits, with_swa=True)
         to = dict(device=device)
         # the full pool is not read by this step: the sliding-window pool takes its place

@@ -90,12 +90,18 @@ def test_reduce_and_metadata_host_validation(lib):
 def test_workspace_and_split_heuristic(lib):
     assert B.pa_workspace_bytes(32, 32, 128, 10) == 2 * 10240 * 4 + 10240 * 128 * 4
     assert B.pa_workspace_bytes(0, 32, 128, 4) == 0
-    for bs, hkv, pages in ((1, 8, 16), (8, 8, 16), (1, 8, 128), (32, 8, 128), (64, 8, 256), (1, 1, 1)):
-        s = B.pa_choose_splits(bs, hkv, pages, 64, 152)
-        assert 1 <= s <= max(1, pages)
-        pps = -(-pages // s)
-        assert -(-pages // pps) == s          # the longest request has no empty split
-    assert B.pa_choose_splits(0, 8, 16, 64, 152) == 1
+    for kv in (B.PA_KV_BF16, B.PA_KV_INT8):
+        for bs, hkv, pages in ((1, 8, 16), (8, 8, 16), (1, 8, 128), (32, 8, 128), (64, 8, 256),
+                               (64, 8, 65), (1, 1, 1)):
+            s = B.pa_choose_splits(bs, hkv, pages, 64, kv, 152)
+            assert 1 <= s <= max(1, pages)
+            pps = -(-pages // s)
+            assert -(-pages // pps) == s          # the longest request has no empty split
+    # the GB300 sweep's best counts: bs32 ctx8K bf16, bs64 ctx16K int8, bs64 window 4096 int8
+    assert B.pa_choose_splits(32, 8, 128, 64, B.PA_KV_BF16, 152) == 5
+    assert B.pa_choose_splits(64, 8, 256, 64, B.PA_KV_INT8, 152) == 4
+    assert B.pa_choose_splits(64, 8, 65, 64, B.PA_KV_INT8, 152) == 3
+    assert B.pa_choose_splits(0, 8, 16, 64, B.PA_KV_BF16, 152) == 1
     assert B.pa_status_string(B.PA_ERR_UNSUPPORTED) == "unsupported shape"
 
 
