@@ -357,7 +357,16 @@ def run_gb300(args, spec, rank, world, local_rank):
     ds = DeviceStep(wl)
     stream = torch.cuda.Stream()
     binding.pa_read_error_flags(reset=True)
-    graph = capture(torch, lambda: ds.step(use_pdl=True), stream)
+    # One graph holds several consecutive steps (PDL chains each step's kernels to the
+    # previous step's, as consecutive layers of a model graph would), so the time per
+    # step is the GPU's and not the host's graph-launch rate.  K is timed exactly:
+    # the steps per graph divide K.
+    per_graph = next(n for n in (8, 4, 2, 1) if args.steps % n == 0)
+
+    def steps():
+        for _ in range(per_graph):
+            ds.step(use_pdl=True)
+    graph = capture(torch, steps, stream)
     if binding.pa_read_error_flags(reset=True):
         raise RuntimeError("device error flags set during warm-up")
 
@@ -365,12 +374,12 @@ def run_gb300(args, spec, rank, world, local_rank):
     if rank == 0:
         sampler.start()
         time.sleep(1.0)
-    for _ in range(max(3, args.warmup)):
+    for _ in range(-(-max(3, args.warmup) // per_graph)):
         graph.replay()
     # keep the GPU busy for ~1.5 s so the clock samples see the loaded state
     t_end = time.time() + 1.5
     while time.time() < t_end:
-        for _ in range(200):
+        for _ in range(max(1, 200 // per_graph)):
             graph.replay()
         torch.cuda.synchronize()
 
@@ -379,7 +388,7 @@ def run_gb300(args, spec, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     sampler.mark("start")
-    us_step = time_graph(torch, graph, args.steps, stream)
+    us_step = time_graph(torch, graph, args.steps // per_graph, stream) / per_graph
     torch.cuda.synchronize()
     sampler.mark("stop")
     if world > 1:
@@ -453,8 +462,12 @@ def run_gb300(args, spec, rank, world, local_rank):
         extras["e2e"] = {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": d2h}
         # ---- same graph without PDL, and the batch-1 PDL study -------------------------
-        g_nopdl = capture(torch, lambda: ds.step(use_pdl=False), stream)
-        extras["graph_no_pdl_us"] = time_graph(torch, g_nopdl, min(args.steps, 2000), stream)
+        def steps_nopdl():
+            for _ in range(per_graph):
+                ds.step(use_pdl=False)
+        g_nopdl = capture(torch, steps_nopdl, stream)
+        extras["graph_no_pdl_us"] = time_graph(
+            torch, g_nopdl, max(1, min(args.steps, 2000) // per_graph), stream) / per_graph
         del g_nopdl
         extras["pdl_bs1"] = pdl_study(torch, synthetic, DeviceStep, stream)
         extras["pdl_gaps_bs1"] = pdl_gap_study(torch, synthetic, DeviceStep, binding, stream)
@@ -472,6 +485,7 @@ def run_gb300(args, spec, rank, world, local_rank):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
         if spec.kv_dtype == "bf16" else "int8", "data": "synthetic",
         "config": dict(workload_config(spec, wl, ds.num_splits), pdl=True, cuda_graph=True,
+                       steps_per_graph=per_graph,
                        l2="inputs larger than L2: %.2f GB of KV per step, no flush" % (kv_bytes / 1e9),
                        parallelism="replicas" if world > 1 else "single GPU"),
         "kv_hbm_gbs": kv_gbs, "kv_hbm_frac": kv_gbs / hbm_peak,

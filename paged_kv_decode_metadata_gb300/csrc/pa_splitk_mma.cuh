@@ -61,6 +61,15 @@ constexpr int kMaxSplitPages = 256;
 #define PA_MAX_SLACK 8
 #endif
 constexpr float kMaxSlack = PA_MAX_SLACK;
+// Full 16-token slices of a one-query, full-context split skip the per-score masks.
+#ifndef PA_MASK_FAST
+#define PA_MASK_FAST 1
+#endif
+// int8 V enters the PV product still biased by +1152 (no per-element subtract); the
+// bias is removed once per split from the column sums of the fp16 weights.
+#ifndef PA_INT8_V_BIAS
+#define PA_INT8_V_BIAS 1
+#endif
 
 template <bool kQuant, int STAGES>
 struct Layout {
@@ -148,8 +157,11 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 
 // Two biased int8 codes (already XORed with 0x80) -> fp16x2 holding the signed codes:
 // each byte becomes the low mantissa byte of 1024, then 1152 is subtracted (exact).
+// kKeepBias: leave the +1152 in (code + 1152, also exact).
+template <bool kKeepBias>
 __device__ __forceinline__ uint32_t biased_bytes_to_f16x2(uint32_t x, uint32_t selector) {
   const uint32_t h = __byte_perm(x, 0x64646464u, selector);
+  if constexpr (kKeepBias) return h;
   __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), __float2half2_rn(1152.f));
   return *reinterpret_cast<uint32_t*>(&v);
 }
@@ -444,6 +456,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
   for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
+  // int8 with the V bias kept: per column, the sum of the fp16 weights that entered the
+  // PV product (every row of the fragment holds the same sums); O = O_biased - 1152 sum.
+  constexpr bool kVBias = kQuant && PA_INT8_V_BIAS;
+  float wsum[kNT][4];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) wsum[nt][0] = wsum[nt][1] = wsum[nt][2] = wsum[nt][3] = 0.f;
   // softmax state of heads 8*nt + 2*tig + e (identical in the 8 lanes sharing tig)
   // m_run: the reference maximum the weights are relative to (warp-uniform per column);
   // t_max: this thread's true maximum of its own scores, reduced once per split.
@@ -562,6 +580,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
         vs_b = tok_b < valid ? vscale[tok_b] : 0.f;
       }
       uint32_t pb[kNT][2];
+      // every score of a full slice of a one-query split without a window is visible
+      // (columns past the request's heads carry zero queries and are never written)
+      const bool need_mask = !PA_MASK_FAST || partial || multi || check_lo;
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) {
         float x[4];  // (token a, head e0), (a, e1), (b, e0), (b, e1)
@@ -571,10 +592,16 @@ __global__ void __launch_bounds__(kThreads, MINB)
           if constexpr (kQuant) v -= kbias[nt][i & 1];
           v *= q_scale;
           if constexpr (kQuant) v *= (i < 2 ? ks_a : ks_b);
-          const int pos = c * kChunk + (i < 2 ? tok_a : tok_b);  // position in the split
-          bool seen = (i < 2 ? tok_a : tok_b) < valid && pos < lim[nt][i & 1];
-          if (check_lo) seen = seen && pos >= lim[nt][i & 1] - window;
-          x[i] = seen ? v : -CUDART_INF_F;
+          x[i] = v;
+        }
+        if (need_mask) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int pos = c * kChunk + (i < 2 ? tok_a : tok_b);  // position in the split
+            bool seen = (i < 2 ? tok_a : tok_b) < valid && pos < lim[nt][i & 1];
+            if (check_lo) seen = seen && pos >= lim[nt][i & 1] - window;
+            x[i] = seen ? x[i] : -CUDART_INF_F;
+          }
         }
         // Reference maximum per column, moved only when a score exceeds it by more than
         // 2^kMaxSlack (one vote instead of a shuffle reduction and a rescale per slice);
@@ -605,6 +632,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
               o[nt][i][1] *= alpha[1];
               o[nt][i][2] *= alpha[0];
               o[nt][i][3] *= alpha[1];
+            }
+            if constexpr (kVBias) {
+              wsum[nt][0] *= alpha[0];
+              wsum[nt][1] *= alpha[1];
+              wsum[nt][2] *= alpha[0];
+              wsum[nt][3] *= alpha[1];
             }
           }
         }
@@ -647,15 +680,25 @@ __global__ void __launch_bounds__(kThreads, MINB)
           const uint32_t xc = wc[w] ^ 0x80808080u, xd = wd[w] ^ 0x80808080u;
           const uint32_t ab_lo = __byte_perm(xa, xb, 0x5140), ab_hi = __byte_perm(xa, xb, 0x7362);
           const uint32_t cd_lo = __byte_perm(xc, xd, 0x5140), cd_hi = __byte_perm(xc, xd, 0x7362);
-          uint32_t a_even[4] = {biased_bytes_to_f16x2(ab_lo, 0x4140), biased_bytes_to_f16x2(ab_lo, 0x4342),
-                                biased_bytes_to_f16x2(cd_lo, 0x4140), biased_bytes_to_f16x2(cd_lo, 0x4342)};
-          uint32_t a_odd[4] = {biased_bytes_to_f16x2(ab_hi, 0x4140), biased_bytes_to_f16x2(ab_hi, 0x4342),
-                               biased_bytes_to_f16x2(cd_hi, 0x4140), biased_bytes_to_f16x2(cd_hi, 0x4342)};
+          uint32_t a_even[4] = {biased_bytes_to_f16x2<kVBias>(ab_lo, 0x4140),
+                                biased_bytes_to_f16x2<kVBias>(ab_lo, 0x4342),
+                                biased_bytes_to_f16x2<kVBias>(cd_lo, 0x4140),
+                                biased_bytes_to_f16x2<kVBias>(cd_lo, 0x4342)};
+          uint32_t a_odd[4] = {biased_bytes_to_f16x2<kVBias>(ab_hi, 0x4140),
+                               biased_bytes_to_f16x2<kVBias>(ab_hi, 0x4342),
+                               biased_bytes_to_f16x2<kVBias>(cd_hi, 0x4140),
+                               biased_bytes_to_f16x2<kVBias>(cd_hi, 0x4342)};
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt) {
             mma16816<true>(o[nt][2 * w], a_even, pb[nt][0], pb[nt][1]);
             mma16816<true>(o[nt][2 * w + 1], a_odd, pb[nt][0], pb[nt][1]);
           }
+        }
+        if constexpr (kVBias) {
+          // column sums of the fp16 weights: an all-ones A operand (fp16 1.0 = 0x3C00)
+          const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) mma16816<true>(wsum[nt], ones, pb[nt][0], pb[nt][1]);
         }
       } else {
         const int mi = lane >> 3;
@@ -735,8 +778,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int i = 0; i < 8; ++i) {
           const int ch0 = kQuant ? 16 * gid + 2 * i : 16 * i + gid;
           const int ch1 = kQuant ? 16 * gid + 2 * i + 1 : 16 * i + gid + 8;
-          dst[ch0] = o[nt][i][e] * scale;
-          dst[ch1] = o[nt][i][2 + e] * scale;
+          float v0 = o[nt][i][e], v1 = o[nt][i][2 + e];
+          if constexpr (kVBias) {
+            v0 -= 1152.f * wsum[nt][e];
+            v1 -= 1152.f * wsum[nt][2 + e];
+          }
+          dst[ch0] = v0 * scale;
+          dst[ch1] = v1 * scale;
         }
       }
     }
