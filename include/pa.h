@@ -6,11 +6,15 @@
  *   pa_build_metadata  -> pa_decode_splitk  -> pa_reduce
  *   (fused metadata)      (split-K producer)   (log-sum-exp reducer)
  *
- * pa_decode_step issues all three.  Every entry point takes plain device pointers
+ * pa_decode_step issues all three; pa_decode_splitk_multi (several query tokens per
+ * request) and pa_decode_splitk_window / pa_decode_step_window (sliding-window layers)
+ * are the producer's other forms.  Every entry point takes plain device pointers
  * and sizes, enqueues work on `stream` (a cudaStream_t passed as void*, NULL = the
  * legacy default stream) and returns without synchronising.  No entry point
- * allocates memory: the caller owns every buffer, including the split-K scratch.
- * All launches are capturable into a CUDA graph.  When use_pdl is non-zero the
+ * allocates memory: the caller owns every buffer, including the split-K scratch
+ * (pa_decode_step_static_scratch uses a scratch array inside the library instead).
+ * The metadata, producer, reducer and pa_decode_step(_window) launches are recorded
+ * into CUDA graphs by this library's benchmark and tests.  When use_pdl is non-zero the
  * kernel is launched with the programmatic-stream-serialisation attribute, so it
  * may start while the previous kernel in the stream finishes; each kernel waits
  * (griddepcontrol.wait) before it reads anything an earlier kernel wrote.
