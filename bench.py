@@ -183,6 +183,20 @@ def cpu_baseline(wl, budget_s=10.0):
                       f"scaled to the step's {total_tokens} tokens"}
 
 
+def max_over_ranks(value, world, device="cpu"):
+    """The largest of each rank's `value` (every rank gets it); `value` on one rank.
+    Uses the default process group, so `device` must suit its backend (cuda for nccl,
+    cpu for gloo)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, spec, rank, world):
     """The oracle as the reference arm: each step is a bounded sample of the workload."""
     if rank != 0:
@@ -393,9 +407,7 @@ def run_gb300(args, spec, rank, world, local_rank):
     sampler.mark("stop")
     if world > 1:
         dist.barrier()
-        t = torch.tensor([us_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        us_step = float(t.item())
+    us_step = max_over_ranks(us_step, world, "cuda")
     clocks = sampler.stop() if rank == 0 else None
 
     # ---- dominant kernel alone: the split-K producer, CUDA events on its stream -------

@@ -65,6 +65,47 @@ def test_splitk_host_validation(lib):
         assert _splitk(lib, hq=128) == B.PA_ERR_UNSUPPORTED   # group 16: tensor-core only
 
 
+def _window(lib, **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, ks=None, vs=None, kv=0, pt=FAKE, pts=16, cl=FAKE, cq=None,
+             bs=2, mql=1, hq=32, hkv=8, d=128, P=64, pages=100, msp=16, W=100, S=4, scale=0.1,
+             m=FAKE, l=FAKE, acc=FAKE)
+    a.update(over)
+    return lib.pa_decode_splitk_window(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["kv"], a["pt"],
+                                       a["pts"], a["cl"], a["cq"], a["bs"], a["mql"], a["hq"],
+                                       a["hkv"], a["d"], a["P"], a["pages"], a["msp"], a["W"],
+                                       a["S"], a["scale"], a["m"], a["l"], a["acc"], None, 1)
+
+
+def test_window_host_validation(lib):
+    assert _window(lib, bs=0) == B.PA_OK
+    assert _window(lib, W=0) == B.PA_ERR_INVALID
+    assert _window(lib, W=-3) == B.PA_ERR_INVALID
+    assert _window(lib, q=None) == B.PA_ERR_INVALID
+    assert _window(lib, msp=1 << 24, pts=1 << 24) == B.PA_ERR_UNSUPPORTED  # positions > 2^29
+    assert _window(lib, cq=FAKE, mql=0) == B.PA_ERR_INVALID
+    assert _window(lib, cq=FAKE, mql=3, hq=64) == B.PA_ERR_UNSUPPORTED       # 8 heads x 3 > 16
+    with B.producer(B.PA_PRODUCER_FMA):
+        assert _window(lib) == B.PA_ERR_UNSUPPORTED                       # tensor-core only
+    step = lambda **o: lib.pa_decode_step_window(
+        FAKE, FAKE, FAKE, 4, 1024, o.get("map", FAKE), 100, 0, 16, FAKE, FAKE, FAKE, 16,
+        o.get("swa", FAKE), 16, FAKE, FAKE, FAKE, None, None, 0, 2, 32, 8, 128, 64, 100,
+        o.get("W", 100), 4, 0.1, FAKE, 1 << 20, FAKE, None, None, 1)
+    assert step(W=0) == B.PA_ERR_INVALID
+    assert step(map=None, swa=None) == B.PA_ERR_INVALID                   # needs the SWA table
+
+
+def test_window_pages():
+    # the most pages W + max_q_len - 1 consecutive positions can touch, capped
+    assert B.pa_window_pages(4096, 1, 64, 256) == 65
+    assert B.pa_window_pages(4096, 1, 64, 40) == 40
+    assert B.pa_window_pages(6, 3, 4, 4) == 3
+    assert B.pa_window_pages(8, 3, 4, 4) == 4
+    assert B.pa_window_pages(1, 1, 16, 100) == 2
+    assert B.pa_window_pages(64, 1, 64, 100) == 2
+    assert B.pa_window_pages(0, 1, 64, 100) == 0
+    assert B.pa_window_pages(10, 0, 64, 100) == 0
+
+
 def test_producer_selection(lib):
     prev = B.pa_select_producer(B.PA_PRODUCER_FMA)
     assert B.pa_select_producer(B.PA_PRODUCER_MMA) == B.PA_PRODUCER_FMA
