@@ -269,6 +269,7 @@ pa_status decode_splitk_impl(const void* q, const void* k_cache, const void* v_c
   p.max_seq_pages = max_seq_pages;
   p.pages_per_split = static_cast<int32_t>(cdiv(split_pages, num_splits));
   p.window = window;
+  p.sm_count = sm_count_of_current_device();
   p.num_splits = num_splits;
   p.q_scale = sm_scale * 1.4426950408889634f;  // log2(e): the kernel works in base 2
   p.cu_seqlens_q = cu_seqlens_q;

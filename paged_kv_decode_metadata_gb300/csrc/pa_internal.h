@@ -63,6 +63,8 @@ struct SplitKParams {
   // request's first visible position, and skips pages whose table entry is -1.
   // pages_per_split is then counted over the window's pages.  0: whole context.
   int32_t window;
+  int32_t sm_count;  // SMs of the device (grids of at most this many blocks take the
+                     // deep-pipeline configuration)
   float* m_out;
   float* l_out;
   float* acc_out;

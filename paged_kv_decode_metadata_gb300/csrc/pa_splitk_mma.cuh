@@ -886,7 +886,10 @@ cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const C
 
 // (STAGES, MINB) for G <= 8 (one n-tile of heads) and for G = 16 (two n-tiles, more
 // registers per thread).
-template <bool kQuant, int STAGES1, int MINB1, int STAGES2, int MINB2, bool kWindow>
+// STAGES_DEEP > 0: grids of at most p.sm_count blocks with one n-tile use STAGES_DEEP
+// stages and one CTA per SM.
+template <bool kQuant, int STAGES1, int MINB1, int STAGES2, int MINB2, int STAGES_DEEP,
+          bool kWindow>
 cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_size,
                             cudaStream_t stream, bool use_pdl) {
   CUtensorMap mk, mv;
@@ -897,8 +900,15 @@ cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_s
   const dim3 grid(static_cast<unsigned>(p.num_splits), static_cast<unsigned>(p.num_kv_heads),
                   static_cast<unsigned>(bs));
   const bool two_tiles = group * (p.cu_seqlens_q != nullptr ? p.max_q_len : 1) > 8;
+  const bool deep = STAGES_DEEP > 0 && !two_tiles &&
+                    static_cast<int64_t>(grid.x) * grid.y * grid.z <= p.sm_count;
 #define PA_MMA_CASE(PP)                                                                        \
   if (page_size == PP) {                                                                       \
+    if constexpr (STAGES_DEEP > 0) {                                                           \
+      if (deep)                                                                                \
+        return launch_mma_one<kQuant, PP, (STAGES_DEEP > 0 ? STAGES_DEEP : 1), 1, 1, kWindow>( \
+            p, mk, mv, grid, stream, use_pdl);                                                 \
+    }                                                                                          \
     return two_tiles                                                                           \
                ? launch_mma_one<kQuant, PP, STAGES2, MINB2, 2, kWindow>(p, mk, mv, grid, stream,  \
                                                                          use_pdl)               \

@@ -32,3 +32,16 @@
 #ifndef PA_MMA_INT8_MINB2
 #define PA_MMA_INT8_MINB2 2
 #endif
+
+// Grids of at most one block per SM (batch-1 steps): a deep ring instead, one CTA per SM,
+// so every chunk of a short split is in flight from the start (the split is latency
+// bound, not bandwidth bound).  bf16: four 32 KiB stages; int8: eight 17 KiB stages.
+#ifndef PA_MMA_SMALL_GRID_DEEP
+#define PA_MMA_SMALL_GRID_DEEP 1
+#endif
+#ifndef PA_MMA_BF16_STAGES_DEEP
+#define PA_MMA_BF16_STAGES_DEEP 4
+#endif
+#ifndef PA_MMA_INT8_STAGES_DEEP
+#define PA_MMA_INT8_STAGES_DEEP 8
+#endif
