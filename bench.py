@@ -452,14 +452,12 @@ def run_gb300(args, spec, rank, world, local_rank):
         h_out = torch.empty(ds.out.shape, dtype=ds.out.dtype, **pin)
         h_lse = torch.empty(ds.lse.shape, dtype=ds.lse.dtype, **pin)
 
+        # one C-ABI call per step: pinned host inputs in, the step, host outputs back
+        host_step = ds.prepare_host_step(h_q, h_rpi, h_sl, h_out, h_lse, use_pdl=True,
+                                         stream=stream)
+
         def e2e_step():
-            with torch.cuda.stream(stream):
-                ds.q.copy_(h_q, non_blocking=True)
-                ds.seq_lens.copy_(h_sl, non_blocking=True)
-                ds.req_pool_indices.copy_(h_rpi, non_blocking=True)
-                ds.step(use_pdl=True, stream=stream)
-                h_out.copy_(ds.out, non_blocking=True)
-                h_lse.copy_(ds.lse, non_blocking=True)
+            host_step()
             stream.synchronize()
 
         for _ in range(20):

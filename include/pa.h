@@ -295,6 +295,35 @@ PA_API pa_status pa_decode_step(
     void* stream, int32_t use_pdl);
 
 /*
+ * pa_decode_step_host -- pa_decode_step for callers whose per-step inputs and outputs
+ * live in host memory.  Enqueued on `stream`, in order: three host-to-device copies
+ * (h_q -> q, h_req_pool_indices -> req_pool_indices, h_seq_lens -> seq_lens; q,
+ * req_pool_indices and seq_lens are the caller's device buffers, overwritten here), the
+ * three kernels of pa_decode_step, and two device-to-host copies (out -> h_out,
+ * lse -> h_lse).  Returns without synchronising: the host outputs are valid once the
+ * stream has completed.  h_* should be page-locked (cudaHostAlloc / pinned) for the
+ * copies to be asynchronous; pageable memory works but the copies then block the host.
+ *   h_q    [bs, num_q_heads, head_dim] bf16     h_req_pool_indices, h_seq_lens [bs] int64
+ *   h_out  [bs, num_q_heads, head_dim] bf16     h_lse [bs, num_q_heads] fp32 or NULL
+ *                                               (NULL exactly when lse is NULL)
+ * The remaining arguments are those of pa_decode_step.  Errors: PA_ERR_INVALID for a
+ * NULL host or device buffer, and as pa_decode_step; a failed copy returns PA_ERR_CUDA.
+ */
+PA_API pa_status pa_decode_step_host(
+    const void* h_q, const int64_t* h_req_pool_indices, const int64_t* h_seq_lens,
+    void* h_out, float* h_lse, const int64_t* req_pool_indices, const int64_t* seq_lens,
+    const int32_t* req_to_token, int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const void* q,
+    const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale,
+    int32_t kv_dtype, int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t num_splits,
+    float sm_scale, void* workspace, size_t workspace_bytes, void* out, float* lse,
+    void* stream, int32_t use_pdl);
+
+/*
  * pa_decode_step_window -- pa_decode_step for a sliding-window attention layer: the
  * metadata stage (full_to_swa_mapping and swa_page_table are required here), then
  * pa_decode_splitk_window over swa_page_table with one query per request, then

@@ -102,6 +102,7 @@ def _declare(lib):
     lib.pa_decode_step.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp, vp, vp, i64,
                                    vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                    i64, i32, f32, vp, sz, vp, vp, vp, i32]
+    lib.pa_decode_step_host.argtypes = [vp, vp, vp, vp, vp] + lib.pa_decode_step.argtypes
     lib.pa_decode_step_window.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp, vp, vp,
                                           i64, vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                           i32, i32, i64, i32, i32, f32, vp, sz, vp, vp, vp, i32]
@@ -123,7 +124,8 @@ def _declare(lib):
     lib.pa_read_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     for name in ("pa_build_metadata", "pa_build_metadata_full", "pa_decode_splitk",
                  "pa_decode_splitk_multi", "pa_decode_splitk_window", "pa_reduce",
-                 "pa_decode_step", "pa_decode_step_window", "pa_read_error_flags"):
+                 "pa_decode_step", "pa_decode_step_host", "pa_decode_step_window",
+                 "pa_read_error_flags"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -318,18 +320,23 @@ def pa_reduce(scratch_m, scratch_l, scratch_acc, out, lse=None, *, stream=None,
     _check("pa_reduce", st)
 
 
-def pa_decode_step(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: int,
-                   max_seq_pages: int, cache_seqlens, cu_seqlens_k, page_table, q, k_cache,
-                   v_cache, num_splits: int, sm_scale: float, workspace, out, lse=None,
-                   k_scale=None, v_scale=None, full_to_swa_mapping=None, swa_page_table=None,
-                   stream=None, use_pdl: bool = True, lib=None):
+def pa_decode_step(*, lib=None, **kw):
     """Metadata + split-K producer + reducer in one call; see include/pa.h.  ``lib``
-    selects another build of the library (e.g. ``load_instrumented()``)."""
+    selects another build of the library (e.g. ``load_instrumented()``).  Keyword
+    arguments: those of ``_decode_step_args``."""
     lib = lib or load()
+    _check("pa_decode_step", lib.pa_decode_step(*_decode_step_args(**kw)), lib)
+
+
+def _decode_step_args(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: int,
+                      max_seq_pages: int, cache_seqlens, cu_seqlens_k, page_table, q, k_cache,
+                      v_cache, num_splits: int, sm_scale: float, workspace, out, lse=None,
+                      k_scale=None, v_scale=None, full_to_swa_mapping=None, swa_page_table=None,
+                      stream=None, use_pdl: bool = True):
     kv_dtype, ks, vs = _kv_args(k_cache, v_cache, k_scale, v_scale)
     bs, hq, d = q.shape
     num_pages, hkv, page_size, _ = k_cache.shape
-    st = lib.pa_decode_step(
+    return (
         _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
         _ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
         req_to_token.shape[0], req_to_token.stride(0),
@@ -345,21 +352,54 @@ def pa_decode_step(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: i
         int(num_splits), float(sm_scale), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _ptr(out, torch.bfloat16, "out"),
         _ptr(lse, torch.float32, "lse"), _stream(stream), int(bool(use_pdl)))
-    _check("pa_decode_step", st, lib)
 
 
-def pa_decode_step_window(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: int,
-                          max_seq_pages: int, cache_seqlens, cu_seqlens_k, page_table,
-                          full_to_swa_mapping, swa_page_table, q, k_swa, v_swa,
-                          sliding_window: int, num_splits: int, sm_scale: float, workspace,
-                          out, lse=None, k_swa_scale=None, v_swa_scale=None, stream=None,
-                          use_pdl: bool = True, lib=None):
-    """Metadata + sliding-window producer + reducer in one call; see include/pa.h."""
+def _host_ptr(t, dtype, name):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _decode_step_host_args(*, h_q, h_req_pool_indices, h_seq_lens, h_out, h_lse=None, **kw):
+    return (_host_ptr(h_q, torch.bfloat16, "h_q"),
+            _host_ptr(h_req_pool_indices, torch.int64, "h_req_pool_indices"),
+            _host_ptr(h_seq_lens, torch.int64, "h_seq_lens"),
+            _host_ptr(h_out, torch.bfloat16, "h_out"),
+            _host_ptr(h_lse, torch.float32, "h_lse")) + _decode_step_args(**kw)
+
+
+def pa_decode_step_host(*, lib=None, **kw):
+    """pa_decode_step with host inputs (h_q, h_req_pool_indices, h_seq_lens) and host
+    outputs (h_out, h_lse), copies enqueued on the same stream; see include/pa.h.  The
+    other keyword arguments are those of ``pa_decode_step``."""
     lib = lib or load()
+    _check("pa_decode_step_host", lib.pa_decode_step_host(*_decode_step_host_args(**kw)), lib)
+
+
+def pa_decode_step_window(*, lib=None, **kw):
+    """Metadata + sliding-window producer + reducer in one call; see include/pa.h.
+    Keyword arguments: those of ``_decode_step_window_args``."""
+    lib = lib or load()
+    _check("pa_decode_step_window", lib.pa_decode_step_window(*_decode_step_window_args(**kw)),
+           lib)
+
+
+def _decode_step_window_args(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: int,
+                             max_seq_pages: int, cache_seqlens, cu_seqlens_k, page_table,
+                             full_to_swa_mapping, swa_page_table, q, k_swa, v_swa,
+                             sliding_window: int, num_splits: int, sm_scale: float, workspace,
+                             out, lse=None, k_swa_scale=None, v_swa_scale=None, stream=None,
+                             use_pdl: bool = True):
     kv_dtype, ks, vs = _kv_args(k_swa, v_swa, k_swa_scale, v_swa_scale)
     bs, hq, d = q.shape
     num_pages, hkv, page_size, _ = k_swa.shape
-    st = lib.pa_decode_step_window(
+    return (
         _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
         _ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
         req_to_token.shape[0], req_to_token.stride(0),
@@ -374,7 +414,39 @@ def pa_decode_step_window(*, req_pool_indices, seq_lens, req_to_token, seqlen_of
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream),
         int(bool(use_pdl)))
-    _check("pa_decode_step_window", st, lib)
+
+
+class PreparedCall:
+    """One entry point with its arguments marshalled once: calling it repeats the call
+    on the same tensors, stream and options, without re-validating or re-converting the
+    Python arguments (the tensors must stay alive and in place)."""
+
+    def __init__(self, name: str, args: tuple, lib=None):
+        self.lib = lib or load()
+        self.name = name
+        self.fn = getattr(self.lib, name)
+        self.args = tuple(t(a) if a is not None else None
+                          for t, a in zip(self.fn.argtypes, args))
+
+    def __call__(self):
+        st = self.fn(*self.args)
+        if st != PA_OK:
+            raise PAError(self.name, st, self.lib)
+
+
+def prepare_decode_step(*, lib=None, **kw) -> PreparedCall:
+    """``pa_decode_step`` with the given keyword arguments, marshalled once."""
+    return PreparedCall("pa_decode_step", _decode_step_args(**kw), lib)
+
+
+def prepare_decode_step_host(*, lib=None, **kw) -> PreparedCall:
+    """``pa_decode_step_host`` with the given keyword arguments, marshalled once."""
+    return PreparedCall("pa_decode_step_host", _decode_step_host_args(**kw), lib)
+
+
+def prepare_decode_step_window(*, lib=None, **kw) -> PreparedCall:
+    """``pa_decode_step_window`` with the given keyword arguments, marshalled once."""
+    return PreparedCall("pa_decode_step_window", _decode_step_window_args(**kw), lib)
 
 
 def pa_decode_step_static_scratch(*, req_pool_indices, seq_lens, req_to_token,

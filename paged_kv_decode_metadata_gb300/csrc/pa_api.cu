@@ -502,6 +502,50 @@ pa_status pa_decode_step(
                           workspace_bytes, out, lse, stream, use_pdl);
 }
 
+pa_status pa_decode_step_host(
+    const void* h_q, const int64_t* h_req_pool_indices, const int64_t* h_seq_lens,
+    void* h_out, float* h_lse, const int64_t* req_pool_indices, const int64_t* seq_lens,
+    const int32_t* req_to_token, int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const void* q,
+    const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale,
+    int32_t kv_dtype, int32_t bs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t num_splits,
+    float sm_scale, void* workspace, size_t workspace_bytes, void* out, float* lse,
+    void* stream, int32_t use_pdl) {
+  if (bs < 0 || num_q_heads < 1 || head_dim < 1) return PA_ERR_INVALID;
+  if (bs == 0) return PA_OK;
+  if (!h_q || !h_req_pool_indices || !h_seq_lens || !h_out) return PA_ERR_INVALID;
+  if (!q || !req_pool_indices || !seq_lens || !out) return PA_ERR_INVALID;
+  if ((h_lse == nullptr) != (lse == nullptr)) return PA_ERR_INVALID;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(bs) * num_q_heads;
+  const size_t qo_bytes = rows * static_cast<size_t>(head_dim) * 2;
+  const size_t idx_bytes = static_cast<size_t>(bs) * sizeof(int64_t);
+  cudaError_t e = cudaMemcpyAsync(const_cast<void*>(q), h_q, qo_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<int64_t*>(req_pool_indices), h_req_pool_indices, idx_bytes,
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<int64_t*>(seq_lens), h_seq_lens, idx_bytes,
+                        cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return from_cuda(e, "host-to-device input copy");
+  pa_status st = decode_step_impl(
+      req_pool_indices, seq_lens, req_to_token, req_to_token_rows, req_to_token_stride,
+      full_to_swa_mapping, full_to_swa_mapping_len, seqlen_offset, max_seq_pages, cache_seqlens,
+      cu_seqlens_k, page_table, page_table_stride, swa_page_table, swa_page_table_stride, q,
+      k_cache, v_cache, k_scale, v_scale, kv_dtype, bs, num_q_heads, num_kv_heads, head_dim,
+      page_size, num_pages, 0, num_splits, sm_scale, workspace, workspace_bytes, out, lse, stream,
+      use_pdl);
+  if (st != PA_OK) return st;
+  e = cudaMemcpyAsync(h_out, out, qo_bytes, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && h_lse != nullptr)
+    e = cudaMemcpyAsync(h_lse, lse, rows * sizeof(float), cudaMemcpyDeviceToHost, s);
+  return from_cuda(e, "device-to-host output copy");
+}
+
 pa_status pa_decode_step_window(
     const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
     int64_t req_to_token_rows, int64_t req_to_token_stride,

@@ -61,6 +61,7 @@ class DeviceStep:
         self.out = torch.empty((self.bs, self.num_q_heads, self.head_dim), dtype=torch.bfloat16,
                                device=device)
         self.lse = torch.empty((self.bs, self.num_q_heads), **f32)
+        self._prepared = {}
 
     # ---- the three stages ---------------------------------------------------------
     def metadata(self, use_pdl=True, stream=None):
@@ -86,17 +87,37 @@ class DeviceStep:
         self.splitk(use_pdl, stream)
         self.reduce(use_pdl, stream)
 
+    def _step_kwargs(self):
+        return dict(req_pool_indices=self.req_pool_indices, seq_lens=self.seq_lens,
+                    req_to_token=self.req_to_token, seqlen_offset=self.seqlen_offset,
+                    max_seq_pages=self.max_seq_pages, cache_seqlens=self.cache_seqlens,
+                    cu_seqlens_k=self.cu_seqlens_k, page_table=self.page_table, q=self.q,
+                    k_cache=self.k_cache, v_cache=self.v_cache, num_splits=self.num_splits,
+                    sm_scale=self.sm_scale, workspace=self.workspace, out=self.out,
+                    lse=self.lse, k_scale=self.k_scale, v_scale=self.v_scale,
+                    full_to_swa_mapping=self.full_to_swa_mapping,
+                    swa_page_table=self.swa_page_table)
+
+    _prepare = staticmethod(B.prepare_decode_step)
+
     def step(self, use_pdl=True, stream=None, lib=None):
-        B.pa_decode_step(req_pool_indices=self.req_pool_indices, seq_lens=self.seq_lens,
-                         req_to_token=self.req_to_token, seqlen_offset=self.seqlen_offset,
-                         max_seq_pages=self.max_seq_pages, cache_seqlens=self.cache_seqlens,
-                         cu_seqlens_k=self.cu_seqlens_k, page_table=self.page_table, q=self.q,
-                         k_cache=self.k_cache, v_cache=self.v_cache, num_splits=self.num_splits,
-                         sm_scale=self.sm_scale, workspace=self.workspace, out=self.out,
-                         lse=self.lse, k_scale=self.k_scale, v_scale=self.v_scale,
-                         full_to_swa_mapping=self.full_to_swa_mapping,
-                         swa_page_table=self.swa_page_table, stream=stream, use_pdl=use_pdl,
-                         lib=lib)
+        """One decode step through the C ABI.  The call is marshalled once per (stream,
+        PDL, library) and reused: the buffers above must not be replaced afterwards (in
+        place updates such as ``q.copy_`` are fine)."""
+        key = (B._stream(stream), bool(use_pdl), id(lib))
+        call = self._prepared.get(key)
+        if call is None:
+            call = self._prepare(lib=lib, stream=key[0], use_pdl=use_pdl, **self._step_kwargs())
+            self._prepared[key] = call
+        call()
+
+    def prepare_host_step(self, h_q, h_req_pool_indices, h_seq_lens, h_out, h_lse=None,
+                          use_pdl=True, stream=None):
+        """A prepared ``pa_decode_step_host`` call: host inputs copied into this step's
+        q / req_pool_indices / seq_lens, the step, outputs copied to h_out / h_lse."""
+        return B.prepare_decode_step_host(
+            h_q=h_q, h_req_pool_indices=h_req_pool_indices, h_seq_lens=h_seq_lens, h_out=h_out,
+            h_lse=h_lse, stream=B._stream(stream), use_pdl=use_pdl, **self._step_kwargs())
 
     # ---- accounting -----------------------------------------------------------------
     def kv_bytes(self, ctx) -> int:
@@ -148,18 +169,21 @@ class WindowStep(DeviceStep):
                                   sm_scale=self.sm_scale, k_scale=self.k_scale,
                                   v_scale=self.v_scale, stream=stream, use_pdl=use_pdl)
 
-    def step(self, use_pdl=True, stream=None, lib=None):
-        B.pa_decode_step_window(req_pool_indices=self.req_pool_indices, seq_lens=self.seq_lens,
-                                req_to_token=self.req_to_token, seqlen_offset=self.seqlen_offset,
-                                max_seq_pages=self.max_seq_pages, cache_seqlens=self.cache_seqlens,
-                                cu_seqlens_k=self.cu_seqlens_k, page_table=self.page_table,
-                                full_to_swa_mapping=self.full_to_swa_mapping,
-                                swa_page_table=self.swa_page_table, q=self.q, k_swa=self.k_cache,
-                                v_swa=self.v_cache, sliding_window=self.window,
-                                num_splits=self.num_splits, sm_scale=self.sm_scale,
-                                workspace=self.workspace, out=self.out, lse=self.lse,
-                                k_swa_scale=self.k_scale, v_swa_scale=self.v_scale,
-                                stream=stream, use_pdl=use_pdl, lib=lib)
+    def _step_kwargs(self):
+        return dict(req_pool_indices=self.req_pool_indices, seq_lens=self.seq_lens,
+                    req_to_token=self.req_to_token, seqlen_offset=self.seqlen_offset,
+                    max_seq_pages=self.max_seq_pages, cache_seqlens=self.cache_seqlens,
+                    cu_seqlens_k=self.cu_seqlens_k, page_table=self.page_table,
+                    full_to_swa_mapping=self.full_to_swa_mapping,
+                    swa_page_table=self.swa_page_table, q=self.q, k_swa=self.k_cache,
+                    v_swa=self.v_cache, sliding_window=self.window, num_splits=self.num_splits,
+                    sm_scale=self.sm_scale, workspace=self.workspace, out=self.out,
+                    lse=self.lse, k_swa_scale=self.k_scale, v_swa_scale=self.v_scale)
+
+    _prepare = staticmethod(B.prepare_decode_step_window)
+
+    def prepare_host_step(self, *args, **kwargs):
+        raise NotImplementedError("host-buffer steps cover the full-attention layer only")
 
     def visible_tokens(self, ctx) -> list:
         """Positions each request's query attends: min(n, window)."""

@@ -94,6 +94,20 @@ def test_window_host_validation(lib):
     assert step(map=None, swa=None) == B.PA_ERR_INVALID                   # needs the SWA table
 
 
+def test_host_step_validation(lib):
+    base = [FAKE, FAKE, FAKE, 4, 1024, None, 0, 0, 16, FAKE, FAKE, FAKE, 16, None, 16, FAKE, FAKE,
+            FAKE, None, None, 0, 2, 32, 8, 128, 64, 100, 4, 0.1, FAKE, 1 << 20, FAKE, FAKE, None, 1]
+    host = lambda hq=FAKE, hr=FAKE, hs=FAKE, ho=FAKE, hl=FAKE: lib.pa_decode_step_host(
+        hq, hr, hs, ho, hl, *base)
+    assert host(hq=None) == B.PA_ERR_INVALID
+    assert host(hr=None) == B.PA_ERR_INVALID
+    assert host(ho=None) == B.PA_ERR_INVALID
+    assert host(hl=None) == B.PA_ERR_INVALID                  # lse given, h_lse missing
+    empty = list(base)
+    empty[21] = 0                                             # bs = 0: nothing enqueued
+    assert lib.pa_decode_step_host(None, None, None, None, None, *empty) == B.PA_OK
+
+
 def test_window_pages():
     # the most pages W + max_q_len - 1 consecutive positions can touch, capped
     assert B.pa_window_pages(4096, 1, 64, 256) == 65

@@ -220,6 +220,26 @@ def test_graph_replay_bit_identical_to_eager(use_pdl):
         assert torch.equal(x, y)
 
 
+def test_host_buffer_step_matches_device_step():
+    """pa_decode_step_host: host inputs copied in, the step, outputs copied back; the
+    outputs equal pa_decode_step's bit for bit, on two calls in a row with new inputs."""
+    wl, ds = named("bs8_ctx1k")
+    for call in range(2):
+        q = synthetic.draw_queries(wl.spec.bs, wl.spec.num_q_heads, wl.spec.head_dim, 70 + call)
+        h_q, h_rpi = q.pin_memory(), wl.req_pool_indices.clone().pin_memory()
+        h_sl = wl.seq_lens.clone().pin_memory()
+        h_out = torch.empty(ds.out.shape, dtype=torch.bfloat16).pin_memory()
+        h_lse = torch.empty(ds.lse.shape, dtype=torch.float32).pin_memory()
+        ds.prepare_host_step(h_q, h_rpi, h_sl, h_out, h_lse)()
+        torch.cuda.synchronize()
+        assert torch.equal(ds.q.cpu(), q)
+        ds.step()
+        torch.cuda.synchronize()
+        assert torch.equal(h_out, ds.out.cpu()) and torch.equal(h_lse, ds.lse.cpu())
+    ds.q.copy_(wl.q)
+    _check_flags()
+
+
 def test_page_relabelling_bit_identical_on_gpu():
     spec = synthetic.Spec("relabel", bs=4, num_q_heads=32, num_kv_heads=8, num_pages=80,
                           ragged=(300, 1200), num_splits=5, seed=902)
