@@ -181,3 +181,14 @@ def test_window_rejects_bad_arguments():
             B.pa_decode_splitk_window(*args, sliding_window=10, max_seq_pages=wl.max_seq_pages,
                                       num_splits=2, sm_scale=wl.sm_scale)
     assert e.value.status == B.PA_ERR_UNSUPPORTED
+
+
+def test_window_out_of_range_page_sets_error_flag_without_fault():
+    """A sliding-window table entry past the pool is replaced by a safe page and flagged;
+    nothing outside the pool is read."""
+    wl, meta, table, q, cu_q = _case(24, "int8", 8, 64, 300)
+    b = 2
+    table[b, sorted(wl.swa_pages[b])[-1]] = wl.swa_num_pages + 7
+    B.pa_read_error_flags(reset=True)
+    _run(wl, meta, table, q, cu_q, 2)
+    assert B.pa_read_error_flags(reset=True) & B.DEVERR_PAGE_OUT_OF_RANGE
