@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -60,13 +61,17 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the producer's sources with comments and blank space removed, so that a
+    comment edit does not retire the committed ncu traffic record."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_metadata_gb300", "csrc")
     for name in ("pa_splitk_mma.cuh", "pa_common.cuh", "pa_splitk_mma_config.h",
                  "pa_splitk_mma_bf16.cu", "pa_splitk_mma_int8.cu",
                  "pa_splitk_mma_window_bf16.cu", "pa_splitk_mma_window_int8.cu"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name)) as f:
+            text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(l.strip() for l in text.splitlines() if l.strip()).encode())
     return h.hexdigest()[:16]
 
 

@@ -17,23 +17,31 @@
 //     [num_pages, Hkv, page_size, 128] pools into a STAGES-deep ring; full/empty
 //     mbarriers hand stages back and forth, so there is no CTA-wide barrier per chunk.
 //     128-byte swizzle makes every ldmatrix / 16-byte shared load conflict free.
+//     Grids of at most one block per SM take a deeper ring at one CTA per SM.
 //   * Consumer warp w owns tokens [16w, 16w+16) of every chunk and keeps its own
-//     online-softmax state (max, sum, output) for its tokens; the four states are
-//     merged once at the end of the split (the same log-sum-exp combination the
-//     reducer applies across splits).
-//   * Fragment layout follows the standard flash-attention register reuse: S = Q K^T
-//     with M = 16 query-head rows (rows >= G are zero), N = 8 tokens, K = 16 channels;
-//     the fp32 S fragment becomes, after the softmax, the A fragment of O += P V with
-//     K = 16 tokens, N = 8 channels.  Q fragments stay in registers for the whole split.
-//   * bf16 KV: K fragments come from ldmatrix, V fragments from ldmatrix.trans.
+//     online-softmax state for its tokens; the four states are merged once at the end
+//     of the split (the same log-sum-exp combination the reducer applies across
+//     splits).  The weights of a column are relative to a reference maximum that moves
+//     only when a score passes it by more than 2^kMaxSlack (log2 units), so most slices
+//     need one warp vote instead of a shuffle reduction and a rescale.
+//   * Transposed orientation: S^T = K Q^T with M = 16 tokens, N = 8 columns (a column is
+//     a query head, or a (query, head) pair with several queries per request), K = 16
+//     channels; then O^T += V^T P^T with M = 16 channels, K = 16 tokens, and P^T taken
+//     from the S^T fragments with movmatrix.trans.  Q^T fragments stay in registers for
+//     the whole split.
+//   * bf16 KV: K fragments come from ldmatrix, V^T fragments from ldmatrix.trans.
 //   * int8 KV: 16-byte shared loads of the codes, widened exactly to fp16 in registers
 //     (a byte placed in the mantissa of 1024) and fed to fp16 MMAs (int8 codes are
-//     exact in fp16; Q is rounded to fp16, exact for 2^-14 <= |q| <= 65504).  V codes
-//     are un-biased (minus 1152) before the MMA; K codes enter biased by +1152 and the
-//     resulting 1152 * sum(q) per head is subtracted from the fp32 score.
-//     The contraction order over channels is permuted so that each lane reads
-//     16 contiguous bytes; QK^T does not depend on that order.  The K scale multiplies
-//     the fp32 score, the V scale folds into the softmax weight.
+//     exact in fp16; Q is rounded to fp16, exact for 2^-14 <= |q| <= 65504).  Both K
+//     and V codes enter biased by +1152: the resulting 1152 * sum(q) per column is
+//     subtracted from the fp32 score, and 1152 times each column's sum of fp16 weights
+//     (accumulated by an all-ones MMA) from the output once per split.  The contraction
+//     order over channels is permuted so that each lane reads 16 contiguous bytes;
+//     QK^T does not depend on that order.  The K scale multiplies the fp32 score, the
+//     V scale folds into the softmax weight.
+//   * Sliding window (kWindow): the splits cover each request's window, positions below
+//     a column's window start are masked, and pages with a -1 table entry are neither
+//     loaded nor attended.
 //   * Scores are scaled in fp32 (sm_scale * log2 e), never by rounding Q.
 #pragma once
 
