@@ -160,6 +160,27 @@ def test_split_count_does_not_change_result(splits):
     assert_attention_close(ds.out, ds.lse, out_ref, lse_ref, f"S={splits}")
 
 
+@pytest.mark.parametrize("impl", sorted(PRODUCERS))
+@pytest.mark.parametrize("kv,P,splits", [("bf16", 64, 1), ("int8", 16, 2), ("bf16", 16, 3),
+                                         ("int8", 64, 1)])
+def test_splits_longer_than_the_cached_page_list(kv, P, splits, impl):
+    """Splits of more than 256 pages (up to 1250): the producers cache 256 page indices
+    in shared memory and read the rest from the page table in global memory."""
+    spec = synthetic.Spec(f"long{kv}{P}", bs=2, num_q_heads=16, num_kv_heads=2,
+                          num_pages=2 * (-(-40000 // P)) + 3, ragged=(20000, 40000),
+                          page_size=P, kv_dtype=kv, num_splits=splits, seed=905 + P + splits)
+    wl = synthetic.make(spec)
+    assert -(-wl.max_seq_pages // splits) > 256
+    ds = DeviceStep(wl)
+    with B.producer(PRODUCERS[impl]):
+        ds.step()
+    torch.cuda.synchronize()
+    _check_flags()
+    meta = oracle_metadata(wl)
+    out_ref, lse_ref = oracle_attention(wl, meta)
+    assert_attention_close(ds.out, ds.lse, out_ref, lse_ref, spec.name)
+
+
 def test_empty_and_single_token_requests():
     spec = synthetic.Spec("edge", bs=4, num_q_heads=8, num_kv_heads=2, num_pages=20,
                           ragged=(1, 200), num_splits=3, seed=901)

@@ -192,3 +192,13 @@ def test_window_out_of_range_page_sets_error_flag_without_fault():
     B.pa_read_error_flags(reset=True)
     _run(wl, meta, table, q, cu_q, 2)
     assert B.pa_read_error_flags(reset=True) & B.DEVERR_PAGE_OUT_OF_RANGE
+
+
+def test_window_split_longer_than_the_cached_page_list():
+    """A 20000-token window at page size 16 in one split (1251 pages): page indices past
+    the first 256 come from the sliding-window table in global memory."""
+    wl, meta, table, q, cu_q = _case(25, "bf16", 4, 16, 20000, holes=2, ctx_max=40000)
+    assert B.pa_window_pages(20000, 1, 16, wl.max_seq_pages) > 256
+    out, lse, *_ = _run(wl, meta, table, q, cu_q, 1)
+    out_ref, lse_ref = _oracle(wl, meta, table, q, cu_q)
+    assert_attention_close(out, lse, out_ref, lse_ref, "long window")
