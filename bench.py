@@ -44,6 +44,8 @@ def parse():
                     help="skip the PDL study, e2e and CPU baseline")
     ap.add_argument("--profile", action="store_true",
                     help="eager steps only (warm-up + steps launches of each kernel), for ncu")
+    ap.add_argument("--producer", default="auto", choices=["auto", "mma", "fma"],
+                    help="with --profile: the split-K producer implementation")
     ap.add_argument("--window", action="store_true",
                     help="with --profile: the workload's sliding-window layer step instead")
     ap.add_argument("--all-workloads", action="store_true",
@@ -620,8 +622,11 @@ def run_profile(args, spec):
     else:
         wl = synthetic.make(spec)
         ds = DeviceStep(wl)
-    for _ in range(args.warmup + args.steps):
-        ds.step(use_pdl=True)
+    which = {"auto": binding.PA_PRODUCER_AUTO, "mma": binding.PA_PRODUCER_MMA,
+             "fma": binding.PA_PRODUCER_FMA}[args.producer]
+    with binding.producer(which):
+        for _ in range(args.warmup + args.steps):
+            ds.step(use_pdl=True)
     torch.cuda.synchronize()
     flags = binding.pa_read_error_flags(reset=True)
     if flags:
