@@ -324,6 +324,36 @@ PA_API pa_status pa_decode_step_host(
     void* stream, int32_t use_pdl);
 
 /*
+ * pa_decode_step_multi -- the decode step for several query tokens per request
+ * (speculative target-verify / draft-extend steps): pa_build_metadata_full with the
+ * query side of the metadata module (q_mode PA_Q_MODE_NONE: cu_seqlens_q is preset by
+ * the caller; PA_Q_MODE_CUMSUM: cu_seqlens_q[1:] = cumsum(qlens) (qlens [bs] int64);
+ * PA_Q_MODE_STRIDED: cu_seqlens_q[i] = i * q_stride), then pa_decode_splitk_multi over
+ * those rows, then pa_reduce over the total_q rows.
+ *   q [total_q, num_q_heads, head_dim] bf16, out [total_q, num_q_heads, head_dim] bf16,
+ *   lse [total_q, num_q_heads] fp32 or NULL; total_q must equal cu_seqlens_q[bs] (the
+ *   caller sized q by it); every request has at most max_q_len query rows.
+ * The split-K scratch is carved from `workspace`, which must hold
+ * pa_workspace_bytes(total_q, num_q_heads, head_dim, S), S = num_splits or
+ * pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, kv_dtype, 0).  The other
+ * arguments are those of pa_decode_step.  Errors as the calls it makes; PA_ERR_INVALID
+ * for a NULL cu_seqlens_q or max_q_len < 1.  total_q == 0 runs the metadata stage only.
+ */
+PA_API pa_status pa_decode_step_multi(
+    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
+    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const int64_t* qlens,
+    int32_t q_mode, int32_t q_stride, int32_t* cu_seqlens_q, const void* q, int32_t total_q,
+    int32_t max_q_len, const void* k_cache, const void* v_cache, const float* k_scale,
+    const float* v_scale, int32_t kv_dtype, int32_t bs, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t page_size, int64_t num_pages,
+    int32_t num_splits, float sm_scale, void* workspace, size_t workspace_bytes, void* out,
+    float* lse, void* stream, int32_t use_pdl);
+
+/*
  * pa_decode_step_window -- pa_decode_step for a sliding-window attention layer: the
  * metadata stage (full_to_swa_mapping and swa_page_table are required here), then
  * pa_decode_splitk_window over swa_page_table with one query per request, then

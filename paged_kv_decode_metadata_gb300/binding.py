@@ -103,6 +103,10 @@ def _declare(lib):
                                    vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                    i64, i32, f32, vp, sz, vp, vp, vp, i32]
     lib.pa_decode_step_host.argtypes = [vp, vp, vp, vp, vp] + lib.pa_decode_step.argtypes
+    lib.pa_decode_step_multi.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp, vp, vp,
+                                         i64, vp, i64, vp, i32, i32, vp, vp, i32, i32, vp, vp,
+                                         vp, vp, i32, i32, i32, i32, i32, i32, i64, i32, f32, vp,
+                                         sz, vp, vp, vp, i32]
     lib.pa_decode_step_window.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp, vp, vp,
                                           i64, vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                           i32, i32, i64, i32, i32, f32, vp, sz, vp, vp, vp, i32]
@@ -124,7 +128,8 @@ def _declare(lib):
     lib.pa_read_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     for name in ("pa_build_metadata", "pa_build_metadata_full", "pa_decode_splitk",
                  "pa_decode_splitk_multi", "pa_decode_splitk_window", "pa_reduce",
-                 "pa_decode_step", "pa_decode_step_host", "pa_decode_step_window",
+                 "pa_decode_step", "pa_decode_step_host", "pa_decode_step_multi",
+                 "pa_decode_step_window",
                  "pa_read_error_flags"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
@@ -380,6 +385,41 @@ def pa_decode_step_host(*, lib=None, **kw):
     other keyword arguments are those of ``pa_decode_step``."""
     lib = lib or load()
     _check("pa_decode_step_host", lib.pa_decode_step_host(*_decode_step_host_args(**kw)), lib)
+
+
+def pa_decode_step_multi(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: int,
+                         max_seq_pages: int, cache_seqlens, cu_seqlens_k, page_table,
+                         cu_seqlens_q, q, max_q_len: int, k_cache, v_cache, num_splits: int,
+                         sm_scale: float, workspace, out, lse=None, qlens=None,
+                         q_mode: int = PA_Q_MODE_CUMSUM, q_stride: int = 0, k_scale=None,
+                         v_scale=None, full_to_swa_mapping=None, swa_page_table=None,
+                         stream=None, use_pdl: bool = True):
+    """Metadata (with cu_seqlens_q) + multi-query producer + reducer over the q rows;
+    see include/pa.h."""
+    lib = load()
+    kv_dtype, ks, vs = _kv_args(k_cache, v_cache, k_scale, v_scale)
+    total_q, hq, d = q.shape
+    bs = cache_seqlens.shape[0]
+    num_pages, hkv, page_size, _ = k_cache.shape
+    st = lib.pa_decode_step_multi(
+        _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
+        _ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
+        req_to_token.shape[0], req_to_token.stride(0),
+        _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
+        full_to_swa_mapping.numel() if full_to_swa_mapping is not None else 0,
+        int(seqlen_offset), int(max_seq_pages), _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
+        _ptr(cu_seqlens_k, torch.int32, "cu_seqlens_k"), _ptr2d(page_table, torch.int32, "page_table"),
+        _row_stride(page_table, "page_table"),
+        _ptr2d(swa_page_table, torch.int32, "swa_page_table") if swa_page_table is not None else None,
+        _row_stride(swa_page_table, "swa_page_table") if swa_page_table is not None else 0,
+        _ptr(qlens, torch.int64, "qlens"), int(q_mode), int(q_stride),
+        _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _ptr(q, torch.bfloat16, "q"), total_q,
+        int(max_q_len), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"), ks, vs,
+        kv_dtype, bs, hq, hkv, d, page_size, num_pages, int(num_splits), float(sm_scale),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream),
+        int(bool(use_pdl)))
+    _check("pa_decode_step_multi", st)
 
 
 def pa_decode_step_window(*, lib=None, **kw):

@@ -546,6 +546,63 @@ pa_status pa_decode_step_host(
   return from_cuda(e, "device-to-host output copy");
 }
 
+pa_status pa_decode_step_multi(
+    const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
+    int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const int64_t* qlens,
+    int32_t q_mode, int32_t q_stride, int32_t* cu_seqlens_q, const void* q, int32_t total_q,
+    int32_t max_q_len, const void* k_cache, const void* v_cache, const float* k_scale,
+    const float* v_scale, int32_t kv_dtype, int32_t bs, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t page_size, int64_t num_pages,
+    int32_t num_splits, float sm_scale, void* workspace, size_t workspace_bytes, void* out,
+    float* lse, void* stream, int32_t use_pdl) {
+  if (bs < 0 || total_q < 0 || num_splits < 0) return PA_ERR_INVALID;
+  if (bs == 0) return PA_OK;
+  if (cu_seqlens_q == nullptr || max_q_len < 1) return PA_ERR_INVALID;
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
+    return PA_ERR_INVALID;
+  // the multi-query producer's limits, before anything is enqueued
+  if (g_producer.load() == PA_PRODUCER_FMA ||
+      static_cast<int64_t>(num_q_heads / num_kv_heads) * max_q_len > 16)
+    return PA_ERR_UNSUPPORTED;
+  const int32_t splits =
+      num_splits > 0 ? num_splits
+                     : pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, kv_dtype, 0);
+  if (total_q > 0) {
+    if (!out || !workspace || !aligned16(workspace)) return PA_ERR_INVALID;
+    if (workspace_bytes < pa_workspace_bytes(total_q, num_q_heads, head_dim, splits))
+      return PA_ERR_INVALID;
+  }
+  // the attention arguments are checked before anything is enqueued
+  pa_status st = check_attention(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
+                                 page_table_stride, cache_seqlens, bs, num_q_heads,
+                                 num_kv_heads, head_dim, page_size, num_pages, max_seq_pages,
+                                 splits);
+  if (st != PA_OK) return st;
+  st = pa_build_metadata_full(req_pool_indices, seq_lens, 64, req_to_token, req_to_token_rows,
+                              req_to_token_stride, full_to_swa_mapping,
+                              full_to_swa_mapping_len, nullptr, 0, qlens, cache_seqlens,
+                              cu_seqlens_k, cu_seqlens_q, page_table, page_table_stride,
+                              swa_page_table, swa_page_table_stride, nullptr, 0, bs,
+                              seqlen_offset, max_seq_pages, page_size, q_mode, q_stride, stream,
+                              use_pdl);
+  if (st != PA_OK || total_q == 0) return st;
+  const size_t rows = static_cast<size_t>(total_q) * num_q_heads * splits;
+  char* ws = static_cast<char*>(workspace);
+  float* m = reinterpret_cast<float*>(ws);
+  float* l = reinterpret_cast<float*>(ws + align256(rows * sizeof(float)));
+  float* acc = reinterpret_cast<float*>(ws + 2 * align256(rows * sizeof(float)));
+  st = decode_splitk_impl(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
+                          page_table_stride, cache_seqlens, cu_seqlens_q, max_q_len, bs,
+                          num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                          max_seq_pages, 0, splits, sm_scale, m, l, acc, stream, use_pdl);
+  if (st != PA_OK) return st;
+  return pa_reduce(m, l, acc, total_q, num_q_heads, head_dim, splits, out, lse, stream, use_pdl);
+}
+
 pa_status pa_decode_step_window(
     const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
     int64_t req_to_token_rows, int64_t req_to_token_stride,

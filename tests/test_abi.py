@@ -108,6 +108,21 @@ def test_host_step_validation(lib):
     assert lib.pa_decode_step_host(None, None, None, None, None, *empty) == B.PA_OK
 
 
+def test_multi_step_validation(lib):
+    def step(cq=FAKE, mql=2, hq=32, bs=2, total_q=4):
+        return lib.pa_decode_step_multi(
+            FAKE, FAKE, FAKE, 4, 1024, None, 0, 0, 16, FAKE, FAKE, FAKE, 16, None, 16, FAKE,
+            B.PA_Q_MODE_CUMSUM, 0, cq, FAKE, total_q, mql, FAKE, FAKE, None, None, 0, bs, hq, 8,
+            128, 64, 100, 4, 0.1, FAKE, 1 << 30, FAKE, None, None, 1)
+    assert step(bs=0) == B.PA_OK
+    assert step(cq=None) == B.PA_ERR_INVALID
+    assert step(mql=0) == B.PA_ERR_INVALID
+    assert step(hq=30) == B.PA_ERR_INVALID
+    assert step(hq=64, mql=3) == B.PA_ERR_UNSUPPORTED       # 8 heads x 3 queries > 16
+    with B.producer(B.PA_PRODUCER_FMA):
+        assert step() == B.PA_ERR_UNSUPPORTED
+
+
 def test_window_pages():
     # the most pages W + max_q_len - 1 consecutive positions can touch, capped
     assert B.pa_window_pages(4096, 1, 64, 256) == 65

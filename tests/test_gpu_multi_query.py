@@ -125,3 +125,44 @@ def test_multi_query_unsupported_shapes(lib):
     with pytest.raises(B.PAError) as e:
         _run_multi(wl, qlens, q, 2)
     assert e.value.status == B.PA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("q_mode", ["cumsum", "strided", "preset"])
+def test_multi_step_one_call_matches_stages(q_mode):
+    """pa_decode_step_multi (metadata with cu_seqlens_q, multi-query producer, reducer)
+    equals the three calls made one by one, bit for bit, and the oracle."""
+    spec = synthetic.Spec("mqstep", bs=5, num_q_heads=16, num_kv_heads=4, num_pages=120,
+                          ragged=(1, 900), num_splits=3, seqlen_offset=1, seed=51)
+    wl = synthetic.make(spec)
+    dev = "cuda"
+    if q_mode == "strided":
+        qlens = torch.full((spec.bs,), 3, dtype=torch.int64)
+    else:
+        qlens = synthetic.draw_query_lengths(spec.bs, 4, 52)
+    q = synthetic.draw_queries(int(qlens.sum()), spec.num_q_heads, spec.head_dim, 53)
+    out_ref, lse_ref = _run_multi(wl, qlens, q, 3)
+    i32 = dict(dtype=torch.int32, device=dev)
+    bs, msp = spec.bs, wl.max_seq_pages
+    cl, cu, pt = torch.empty(bs, **i32), torch.empty(bs + 1, **i32), torch.empty((bs, msp), **i32)
+    cq = torch.empty(bs + 1, **i32)
+    if q_mode == "preset":
+        cq.copy_(torch.from_numpy(oracle.cu_seqlens_q(qlens.numpy(), bs, 1)))
+    total_q, hq, d = q.shape
+    ws = torch.empty(B.pa_workspace_bytes(total_q, hq, d, 3), dtype=torch.uint8, device=dev)
+    out = torch.empty((total_q, hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((total_q, hq), dtype=torch.float32, device=dev)
+    mode = {"cumsum": B.PA_Q_MODE_CUMSUM, "strided": B.PA_Q_MODE_STRIDED,
+            "preset": B.PA_Q_MODE_NONE}[q_mode]
+    B.pa_decode_step_multi(req_pool_indices=wl.req_pool_indices.to(dev),
+                           seq_lens=wl.seq_lens.to(dev), req_to_token=wl.req_to_token.to(dev),
+                           seqlen_offset=spec.seqlen_offset, max_seq_pages=msp, cache_seqlens=cl,
+                           cu_seqlens_k=cu, page_table=pt, cu_seqlens_q=cq, q=q.to(dev),
+                           max_q_len=int(qlens.max()), k_cache=wl.k_cache.to(dev),
+                           v_cache=wl.v_cache.to(dev), num_splits=3, sm_scale=wl.sm_scale,
+                           workspace=ws, out=out, lse=lse,
+                           qlens=qlens.to(dev) if q_mode == "cumsum" else None, q_mode=mode,
+                           q_stride=3)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
+    o2, l2 = _oracle_multi(wl, qlens, q)
+    assert_attention_close(out, lse, o2, l2, f"step multi {q_mode}")
