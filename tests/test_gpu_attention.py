@@ -241,6 +241,38 @@ def test_graph_replay_bit_identical_to_eager(use_pdl):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("name", ["bs32_ctx8k", "bs64_ragged16k_int8_swa"])
+def test_benchmark_launch_configuration_matches_oracle(name):
+    """The configuration bench.py times: the full-size workload, the heuristic split
+    count, a CUDA graph of 8 consecutive steps with PDL.  After the replays the outputs
+    equal one eager step bit for bit, and sampled requests match the oracle."""
+    wl, ds = named(name)
+    stream = torch.cuda.Stream()
+
+    def steps():
+        for _ in range(8):
+            ds.step(use_pdl=True)
+    with torch.cuda.stream(stream):
+        steps()
+    torch.cuda.synchronize()
+    eager = _outputs(ds)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        steps()
+    ds.out.zero_()
+    ds.lse.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    _check_flags()
+    for x, y in zip(eager, _outputs(ds)):
+        assert torch.equal(x, y)
+    meta = oracle_metadata(wl)
+    rows = _sample_rows(wl, 4)
+    out_ref, lse_ref = oracle_attention(wl, meta, rows)
+    assert_attention_close(ds.out[rows], ds.lse[rows], out_ref, lse_ref, name + " graph")
+
+
 def test_host_buffer_step_matches_device_step():
     """pa_decode_step_host: host inputs copied in, the step, outputs copied back; the
     outputs equal pa_decode_step's bit for bit, on two calls in a row with new inputs."""
