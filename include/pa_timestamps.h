@@ -29,6 +29,15 @@ extern "C" {
  */
 PA_API pa_status pa_set_timestamp_buffer(uint64_t* buffer);
 
+/*
+ * Failure-detection test hook: with hold != 0, later tensor-core producer launches
+ * issue no copies, so each consumer's wait on its first stage gives up after the wait
+ * limit (~2 s), the kernel sets PA_DEVERR_WAIT_TIMEOUT in the error word, drains (also
+ * bounded) and returns without writing partials; the context stays usable.  hold = 0
+ * restores normal launches.
+ */
+PA_API pa_status pa_set_test_hold_loads(int32_t hold);
+
 #ifdef __cplusplus
 }
 #endif

@@ -76,6 +76,8 @@ def load_instrumented() -> ctypes.CDLL:
             lib = _declare(ctypes.CDLL(path))
             lib.pa_set_timestamp_buffer.argtypes = [ctypes.c_void_p]
             lib.pa_set_timestamp_buffer.restype = ctypes.c_int
+            lib.pa_set_test_hold_loads.argtypes = [ctypes.c_int32]
+            lib.pa_set_test_hold_loads.restype = ctypes.c_int
             _ts_lib = lib
     return _ts_lib
 
@@ -555,8 +557,10 @@ def pa_status_string(status: int) -> str:
     return status_string(status)
 
 
-def pa_read_error_flags(reset: bool = True) -> int:
-    """Device error word (synchronises the device); see include/pa.h."""
+def pa_read_error_flags(reset: bool = True, lib=None) -> int:
+    """Device error word (synchronises the device); see include/pa.h.  ``lib`` reads the
+    word of another build of the library (each build has its own)."""
     v = ctypes.c_uint32(0)
-    _check("pa_read_error_flags", load().pa_read_error_flags(ctypes.byref(v), int(bool(reset))))
+    lib = lib or load()
+    _check("pa_read_error_flags", lib.pa_read_error_flags(ctypes.byref(v), int(bool(reset))), lib)
     return int(v.value)

@@ -22,6 +22,8 @@ std::atomic<unsigned int*> g_err_ptr[kMaxDevices];
 std::atomic<int32_t> g_producer{PA_PRODUCER_AUTO};
 // Stage timestamp buffer (9 uint64) of the instrumented build; nullptr otherwise.
 std::atomic<unsigned long long*> g_ts{nullptr};
+// Instrumented build: non-zero makes later producer launches issue no copies.
+std::atomic<int32_t> g_hold_loads{0};
 std::atomic<int> g_sm_count[kMaxDevices];
 
 cudaError_t error_word(unsigned int** out) {
@@ -270,6 +272,7 @@ pa_status decode_splitk_impl(const void* q, const void* k_cache, const void* v_c
   p.pages_per_split = static_cast<int32_t>(cdiv(split_pages, num_splits));
   p.window = window;
   p.sm_count = sm_count_of_current_device();
+  p.hold_loads = g_hold_loads.load();
   p.num_splits = num_splits;
   p.q_scale = sm_scale * 1.4426950408889634f;  // log2(e): the kernel works in base 2
   p.cu_seqlens_q = cu_seqlens_q;
@@ -630,6 +633,11 @@ pa_status pa_decode_step_window(
 // Instrumented build only (include/pa_timestamps.h).
 pa_status pa_set_timestamp_buffer(uint64_t* buffer) {
   g_ts.store(reinterpret_cast<unsigned long long*>(buffer));
+  return PA_OK;
+}
+
+pa_status pa_set_test_hold_loads(int32_t hold) {
+  g_hold_loads.store(hold != 0 ? 1 : 0);
   return PA_OK;
 }
 #endif

@@ -65,6 +65,7 @@ struct SplitKParams {
   int32_t window;
   int32_t sm_count;  // SMs of the device (grids of at most this many blocks take the
                      // deep-pipeline configuration)
+  int32_t hold_loads;  // instrumented build only: the TMA warp issues nothing (timeout test)
   float* m_out;
   float* l_out;
   float* acc_out;

@@ -351,6 +351,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
   // ======================= producer warp: TMA issue loop ============================
   if (!is_consumer) {
+#ifdef PA_TIMESTAMPS
+    // failure-detection test of the instrumented build: nothing is issued, so every
+    // consumer wait gives up after its time limit and the kernel reports it
+    if (prm.hold_loads) {
+      trigger_dependents();
+      return;
+    }
+#endif
     if (lane == 0) {
       const uint64_t policy = l2_evict_first_policy();
       for (int c = 0; c < n_chunks; ++c) {
