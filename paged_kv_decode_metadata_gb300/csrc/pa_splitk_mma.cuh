@@ -291,7 +291,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
   grid_dependency_wait();
   PA_TS_FIRST(prm.ts, 1, kTsReady);
 
-
   int q_begin = b, q_len = 1;
   if (multi) {
     q_begin = prm.cu_seqlens_q[b];
