@@ -173,11 +173,11 @@ def oracle_sample_us(wl, tokens, request):
     return (time.perf_counter() - t0) * 1e6, n
 
 
-def cpu_baseline_all_cores(wl, budget_s=10.0):
-    """The oracle, unchanged, on whole decode steps with the requests spread over every
-    host core (one request, all its heads, per task; the oracle's C calls release the
-    interpreter lock).  Whole steps are repeated until ~budget_s of wall time (at least
-    one).  Returns (us per step, threads, steps timed)."""
+def oracle_step_runner(wl):
+    """A callable that runs the oracle, unchanged, over one whole decode step of the
+    workload with one request (all its heads) per task on every host core (the oracle's
+    C calls release the interpreter lock); returns (callable, threads).  The callable's
+    ``pool`` attribute is the thread pool (a context manager)."""
     import concurrent.futures
 
     import numpy as np
@@ -197,14 +197,26 @@ def cpu_baseline_all_cores(wl, budget_s=10.0):
         k, v, ks, vs = bits(wl.k_cache), bits(wl.v_cache), None, None
     q, pt, cl = bits(wl.q), meta["page_table"], meta["cache_seqlens"]
     threads = os.cpu_count() or 1
+    pool = concurrent.futures.ThreadPoolExecutor(threads)
 
     def one(r):
         oracle.paged_attention(q[r:r + 1], k, v, pt[r:r + 1], cl[r:r + 1], wl.sm_scale, ks, vs)
 
-    with concurrent.futures.ThreadPoolExecutor(threads) as ex:
+    def run_step():
+        list(pool.map(one, range(wl.spec.bs)))
+    run_step.pool = pool
+    return run_step, threads
+
+
+def cpu_baseline_all_cores(wl, budget_s=10.0):
+    """Whole decode steps of the oracle on every host core (``oracle_step_runner``),
+    repeated until ~budget_s of wall time (at least one, at most five).  Returns
+    (us per step, threads, steps timed)."""
+    run_step, threads = oracle_step_runner(wl)
+    with run_step.pool:
         steps, t0 = 0, time.perf_counter()
         while steps == 0 or (time.perf_counter() - t0 < budget_s and steps < 5):
-            list(ex.map(one, range(wl.spec.bs)))
+            run_step()
             steps += 1
         wall = time.perf_counter() - t0
     return wall / steps * 1e6, threads, steps
@@ -255,46 +267,53 @@ def max_over_ranks(value, world, device="cpu"):
 
 
 def run_reference(args, spec, rank, world):
-    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    """The oracle as the reference arm: every step is one whole decode step of the
+    workload (all requests, all heads, every cached token), the requests spread over
+    every host core, timed as it stands.  Rank 0 alone runs it."""
     if rank != 0:
         return
     from paged_kv_decode_metadata_gb300 import synthetic
 
     wl = synthetic.make(spec)
-    tokens = 256
-    for i in range(args.warmup):
-        oracle_sample_us(wl, tokens, i % spec.bs)
-    per_token = []
-    for i in range(args.steps):
-        us, n = oracle_sample_us(wl, tokens, i % spec.bs)
-        per_token.append(us / n)
-    per_step_us = statistics.mean(per_token) * sum(wl.ctx)
+    run_step, threads = oracle_step_runner(wl)
+    with run_step.pool:
+        for _ in range(max(1, args.warmup)):
+            run_step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            run_step()
+        wall = time.perf_counter() - t0
+    per_step_us = wall / args.steps * 1e6
     line = {
         "impl": "reference", "metric": METRIC, "value": per_step_us, "unit": "us/step",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_step_us / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(spec, wl, None),
-        "cpu_baseline": {"value": per_step_us, "unit": "us/step", "cores": 1, "kind": "oracle",
-                         "sample": f"per step: first {tokens} cached tokens of one request, all "
-                                   f"{spec.num_q_heads} query heads; scaled by {sum(wl.ctx)} "
-                                   "tokens per step"},
+        "config": workload_config(spec, wl),
+        "cpu_baseline": {"value": per_step_us, "unit": "us/step", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{args.steps} whole step(s) after {max(1, args.warmup)} "
+                                   f"warm-up: {spec.bs} requests x {spec.num_q_heads} query "
+                                   f"heads over {sum(wl.ctx)} cached tokens, one request per "
+                                   f"task on {threads} threads"},
         "e2e": {"value": per_step_us, "unit": "us/step", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def workload_config(spec, wl, num_splits):
+def workload_config(spec, wl):
+    """The workload (the same dict on the GPU line and the reference arm's line)."""
     cfg = {"workload": spec.name, "bs": spec.bs,
            "ctx": spec.ctx if spec.ragged is None else f"U[{spec.ragged[0]},{spec.ragged[1]}]",
            "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
            "head_dim": spec.head_dim, "page_size": spec.page_size, "kv_dtype": spec.kv_dtype,
            "seqlen_offset": spec.seqlen_offset}
-    if num_splits is not None:
-        cfg["num_splits"] = num_splits
     if spec.swa_window is not None:
         cfg["swa_window"] = spec.swa_window
+    kv_gb = sum(wl.ctx) * spec.num_kv_heads * 2 * spec.head_dim * (
+        1 if spec.kv_dtype == "int8" else 2) / 1e9
+    cfg["l2"] = "inputs larger than L2: %.2f GB of KV per step, no flush" % kv_gb
     return cfg
 
 
@@ -469,64 +488,24 @@ def run_gb300(args, spec, rank, world, local_rank):
 
     # ---- dominant kernel alone: the split-K producer, CUDA events on its stream -------
     n_kernel = max(20, min(args.steps, 500))
-
-    def producer_us():
-        with torch.cuda.stream(stream):
-            ds.metadata(use_pdl=False)
-            for _ in range(5):
-                ds.splitk(use_pdl=False)
-            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            start.record(stream)
-            for _ in range(n_kernel):
-                ds.splitk(use_pdl=False)
-            end.record(stream)
-        end.synchronize()
-        return start.elapsed_time(end) / n_kernel * 1e3
-
-    splitk_us = producer_us()
+    splitk_us = producer_launch_us(torch, ds, stream, n_kernel)
     producer_alt = {}
     if spec.num_q_heads // spec.num_kv_heads <= 8:
         with binding.producer(binding.PA_PRODUCER_FMA):
-            producer_alt["fma_us"] = producer_us()
+            producer_alt["fma_us"] = producer_launch_us(torch, ds, stream, n_kernel)
 
     kv_bytes = ds.kv_bytes(wl.ctx)
-    rows = spec.bs * spec.num_q_heads
-    # KV (+ int8 scales) read, Q read, partials written, page table and lengths read
-    splitk_bytes = (kv_bytes + rows * spec.head_dim * 2
-                    + rows * ds.num_splits * (spec.head_dim + 2) * 4
-                    + spec.bs * (4 + wl.max_seq_pages * 4))
+    splitk_bytes = producer_bytes(ds, wl, [-(-int(n) // spec.page_size) for n in wl.ctx])
     achieved = splitk_bytes / (splitk_us * 1e-6) / 1e9
     traffic = ncu_traffic(spec.name)
     step_bytes = ds.step_bytes(wl.ctx)
 
     extras = {}
     if rank == 0 and not args.no_extras:
-        # ---- end to end through the public C ABI with host buffers --------------------
-        pin = dict(pin_memory=True)
-        h_q = wl.q.clone().pin_memory()
-        h_sl = wl.seq_lens.clone().pin_memory()
-        h_rpi = wl.req_pool_indices.clone().pin_memory()
-        h_out = torch.empty(ds.out.shape, dtype=ds.out.dtype, **pin)
-        h_lse = torch.empty(ds.lse.shape, dtype=ds.lse.dtype, **pin)
-
-        # one C-ABI call per step: pinned host inputs in, the step, host outputs back
-        host_step = ds.prepare_host_step(h_q, h_rpi, h_sl, h_out, h_lse, use_pdl=True,
-                                         stream=stream)
-
-        def e2e_step():
-            host_step()
-            stream.synchronize()
-
-        for _ in range(20):
-            e2e_step()
-        n_e2e = max(20, min(args.steps, 2000))
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            e2e_step()
-        e2e_us = (time.perf_counter() - t0) / n_e2e * 1e6
-        h2d = h_q.numel() * 2 + h_sl.numel() * 8 + h_rpi.numel() * 8
-        d2h = h_out.numel() * 2 + h_lse.numel() * 4
-        extras["e2e"] = {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
+        # ---- end to end through the public C ABI with host buffers: one call per step,
+        # pinned host inputs in (one copy), the three kernels, outputs back (one copy)
+        us, h2d, d2h = e2e_us(torch, ds, stream, max(20, min(args.steps, 2000)))
+        extras["e2e"] = {"value": us, "unit": "us/step", "h2d_bytes_per_step": h2d,
                          "d2h_bytes_per_step": d2h}
         # ---- same graph without PDL, and the batch-1 PDL study -------------------------
         def steps_nopdl():
@@ -538,6 +517,19 @@ def run_gb300(args, spec, rank, world, local_rank):
         del g_nopdl
         extras["pdl_bs1"] = pdl_study(torch, synthetic, DeviceStep, stream)
         extras["pdl_gaps_bs1"] = pdl_gap_study(torch, synthetic, DeviceStep, binding, stream)
+        # ---- every other workload of the path: graph +/- PDL, eager, L2-rotated for the
+        # small ones; the int8 batch and its sliding-window layer with their producer
+        # roofline (and the int8 batch end to end)
+        l2_bytes = torch.cuda.get_device_properties(local_rank).L2_cache_size
+        table = []
+        for name, window in all_rows(synthetic):
+            if name == spec.name and not window:
+                continue
+            big = synthetic.WORKLOADS[name].kv_dtype == "int8"
+            table.append(measure_workload(torch, name, window, stream, args.steps, hbm_peak,
+                                          peak_kind, l2_bytes, with_producer=big,
+                                          with_e2e=big and not window))
+        extras["workloads"] = table
         extras["cpu_baseline"] = cpu_baseline(wl)
 
     flags = binding.pa_read_error_flags(reset=True)
@@ -551,10 +543,10 @@ def run_gb300(args, spec, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_step / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
         if spec.kv_dtype == "bf16" else "int8", "data": "synthetic",
-        "config": dict(workload_config(spec, wl, ds.num_splits), pdl=True, cuda_graph=True,
-                       steps_per_graph=per_graph,
-                       l2="inputs larger than L2: %.2f GB of KV per step, no flush" % (kv_bytes / 1e9),
-                       parallelism="replicas" if world > 1 else "single GPU"),
+        "config": workload_config(spec, wl),
+        "method": {"num_splits": ds.num_splits, "pdl": True, "cuda_graph": True,
+                   "steps_per_graph": per_graph,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
         "kv_hbm_gbs": kv_gbs, "kv_hbm_frac": kv_gbs / hbm_peak,
         "step_hbm_gbs": step_bytes / (us_step * 1e-6) / 1e9,
         "producer_cuda_core_fma_us": producer_alt.get("fma_us"),
@@ -570,17 +562,149 @@ def run_gb300(args, spec, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def run_table(args):
-    """Per-workload latency table: CUDA graphs holding 8 consecutive steps (so the time
+def producer_launch_us(torch, ds, stream, n):
+    """Average duration of one split-K producer launch: n eager launches without PDL
+    between CUDA events on the launching stream (the metadata stage runs first, once)."""
+    with torch.cuda.stream(stream):
+        ds.metadata(use_pdl=False)
+        for _ in range(5):
+            ds.splitk(use_pdl=False)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(n):
+            ds.splitk(use_pdl=False)
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / n * 1e3
+
+
+def producer_bytes(ds, wl, pages_read):
+    """Algorithmic bytes of one producer launch: KV (+ int8 scales) of the attended
+    tokens, Q read, partials written, page-table entries and lengths read."""
+    spec = wl.spec
+    rows = spec.bs * spec.num_q_heads
+    return (ds.kv_bytes(wl.ctx) + rows * spec.head_dim * 2
+            + rows * ds.num_splits * (spec.head_dim + 2) * 4
+            + spec.bs * 4 + sum(pages_read) * 4)
+
+
+def e2e_us(torch, ds, stream, n):
+    """End to end through pa_decode_step_host: pinned host inputs copied in, the three
+    kernels, outputs copied back, then a stream sync, n times; returns (us per step,
+    h2d bytes, d2h bytes).  The host buffers are laid out like the device groups, so a
+    step makes one copy each way."""
+    h_q, h_rpi, h_sl, h_out, h_lse = ds.host_buffers()
+    h_q.copy_(ds.q)
+    h_rpi.copy_(ds.req_pool_indices)
+    h_sl.copy_(ds.seq_lens)
+    host_step = ds.prepare_host_step(h_q, h_rpi, h_sl, h_out, h_lse, use_pdl=True, stream=stream)
+    for _ in range(20):
+        host_step()
+        stream.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        host_step()
+        stream.synchronize()
+    us = (time.perf_counter() - t0) / n * 1e6
+    h2d = h_q.numel() * 2 + h_sl.numel() * 8 + h_rpi.numel() * 8
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    return us, h2d, d2h
+
+
+def measure_workload(torch, name, window, stream, steps, hbm_peak, peak_kind, l2_bytes,
+                     with_producer=False, with_e2e=False):
+    """One workload's decode step: CUDA graphs holding 8 consecutive steps (so the time
     per step is the GPU's, not the host's graph-launch rate), with and without PDL, and
-    eager C-ABI calls with PDL; KV bandwidth against the measured peak.  Workloads whose
-    per-step bytes fit in 2x the 129 MB L2 are also timed with the inputs rotated over
-    enough copies to exceed 2x L2 (one graph stepping through every copy in turn)."""
+    eager C-ABI calls with PDL.  Steps whose bytes fit in 2x the 129 MB L2 are also
+    timed with the inputs rotated over enough copies to exceed 2x L2 (one graph stepping
+    through every copy in turn).  with_producer: the producer launch alone and its
+    roofline; with_e2e: the end-to-end step through pa_decode_step_host."""
+    from paged_kv_decode_metadata_gb300 import binding, synthetic
+    from paged_kv_decode_metadata_gb300.runtime import DeviceStep, WindowStep
+
+    spec = synthetic.WORKLOADS[name]
+    if window:
+        wl = synthetic.make(spec, with_cache=False, with_swa_cache=True)
+        make_step = lambda: WindowStep(wl)  # noqa: E731
+    else:
+        wl = synthetic.make(spec)
+        make_step = lambda: DeviceStep(wl)  # noqa: E731
+    ds = make_step()
+    per_graph = 8
+    label = name + (f" window {spec.swa_window}" if window else "")
+    row = {"workload": label, "num_splits": ds.num_splits, "steps_per_graph": per_graph}
+    reps = max(20, min(steps, 2000) // per_graph)
+    for pdl in (False, True):
+        def run(pdl=pdl):
+            for _ in range(per_graph):
+                ds.step(use_pdl=pdl)
+        g = capture(torch, run, stream)
+        time_graph(torch, g, 5, stream)
+        row["graph_pdl_us" if pdl else "graph_us"] = min(
+            time_graph(torch, g, reps, stream) for _ in range(3)) / per_graph
+        del g
+    n = max(200, min(steps, 2000))
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            ds.step(use_pdl=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            ds.step(use_pdl=True)
+        b.record(stream)
+    b.synchronize()
+    row["eager_pdl_us"] = a.elapsed_time(b) / n * 1e3
+    footprint = ds.step_bytes(wl.ctx)
+    if footprint < 2 * l2_bytes:
+        copies = int(2 * l2_bytes // footprint) + 1
+        others = [make_step() for _ in range(copies - 1)]
+        everyone = [ds] + others
+
+        def rotate():
+            for d in everyone:
+                d.step(use_pdl=True)
+        g = capture(torch, rotate, stream)
+        time_graph(torch, g, 2, stream)
+        row["graph_pdl_l2_rotated_us"] = min(
+            time_graph(torch, g, max(5, reps // copies), stream) for _ in range(3)) / copies
+        row["l2_rotation_copies"] = copies
+        del g, others, everyone
+    best = row.get("graph_pdl_l2_rotated_us", row["graph_pdl_us"])
+    row["kv_bytes"] = ds.kv_bytes(wl.ctx)
+    row["step_bytes"] = footprint
+    row["kv_gbs"] = row["kv_bytes"] / (best * 1e-6) / 1e9
+    row["kv_frac"] = row["kv_gbs"] / hbm_peak
+    if with_producer:
+        us = producer_launch_us(torch, ds, stream, max(20, min(steps, 500)))
+        P = spec.page_size
+        if window:   # pages holding the window's positions n - v .. n - 1
+            pages = [(n - 1) // P - (n - v) // P + 1 if v > 0 else 0
+                     for n, v in zip(map(int, wl.ctx), ds.visible_tokens(wl.ctx))]
+        else:
+            pages = [-(-int(n) // P) for n in wl.ctx]
+        nbytes = producer_bytes(ds, wl, pages)
+        achieved = nbytes / (us * 1e-6) / 1e9
+        row["roofline"] = {"bound": "hbm", "kernel": "splitk_mma_kernel", "achieved": achieved,
+                           "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                           "frac": achieved / hbm_peak, "traffic": ncu_traffic(label),
+                           "algorithmic_bytes_per_launch": nbytes, "launch_us": us}
+    if with_e2e:
+        us, h2d, d2h = e2e_us(torch, ds, stream, max(20, min(steps, 2000)))
+        row["e2e"] = {"value": us, "unit": "us/step", "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h}
+    if binding.pa_read_error_flags(reset=True):
+        raise RuntimeError("device error flags set")
+    del ds
+    torch.cuda.empty_cache()
+    return row
+
+
+def run_table(args):
+    """Per-workload latency table, one JSON line per workload (not the benchmark line)."""
     import torch
 
     from paged_kv_decode_metadata_gb300 import binding, synthetic
     from paged_kv_decode_metadata_gb300 import build as pa_build
-    from paged_kv_decode_metadata_gb300.runtime import DeviceStep
 
     pa_build.build()
     binding.load()
@@ -588,70 +712,17 @@ def run_table(args):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     stream = torch.cuda.Stream()
     l2_bytes = torch.cuda.get_device_properties(0).L2_cache_size
-    from paged_kv_decode_metadata_gb300.runtime import WindowStep
+    for name, window in all_rows(synthetic):
+        print(json.dumps(measure_workload(torch, name, window, stream, args.steps, hbm_peak,
+                                          peak_kind, l2_bytes, with_producer=True)), flush=True)
 
-    per_graph = 8
-    # every named workload, then the sliding-window layer of the ones that have a window
+
+def all_rows(synthetic):
+    """Every named workload, then the sliding-window layer of those that have one."""
     rows = [(n, False) for n in synthetic.WORKLOAD_ORDER]
     rows += [(n, True) for n in synthetic.WORKLOAD_ORDER
              if synthetic.WORKLOADS[n].swa_window is not None]
-    for name, window in rows:
-        spec = synthetic.WORKLOADS[name]
-        if window:
-            wl = synthetic.make(spec, with_cache=False, with_swa_cache=True)
-            make_step = lambda: WindowStep(wl)  # noqa: E731
-        else:
-            wl = synthetic.make(spec)
-            make_step = lambda: DeviceStep(wl)  # noqa: E731
-        ds = make_step()
-        row = {"workload": name + (f" window {spec.swa_window}" if window else ""),
-               "num_splits": ds.num_splits, "steps_per_graph": per_graph}
-        reps = max(20, min(args.steps, 2000) // per_graph)
-        for pdl in (False, True):
-            def steps(pdl=pdl):
-                for _ in range(per_graph):
-                    ds.step(use_pdl=pdl)
-            g = capture(torch, steps, stream)
-            time_graph(torch, g, 5, stream)
-            row["graph_pdl_us" if pdl else "graph_us"] = min(
-                time_graph(torch, g, reps, stream) for _ in range(3)) / per_graph
-            del g
-        n = max(200, min(args.steps, 2000))
-        with torch.cuda.stream(stream):
-            for _ in range(20):
-                ds.step(use_pdl=True)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(n):
-                ds.step(use_pdl=True)
-            b.record(stream)
-        b.synchronize()
-        row["eager_pdl_us"] = a.elapsed_time(b) / n * 1e3
-        footprint = ds.step_bytes(wl.ctx)
-        if footprint < 2 * l2_bytes:
-            copies = int(2 * l2_bytes // footprint) + 1
-            others = [make_step() for _ in range(copies - 1)]
-            everyone = [ds] + others
-
-            def rotate():
-                for d in everyone:
-                    d.step(use_pdl=True)
-            g = capture(torch, rotate, stream)
-            time_graph(torch, g, 2, stream)
-            row["graph_pdl_l2_rotated_us"] = min(
-                time_graph(torch, g, max(5, reps // copies), stream) for _ in range(3)) / copies
-            row["l2_rotation_copies"] = copies
-            del g, others, everyone
-        best = row.get("graph_pdl_l2_rotated_us", row["graph_pdl_us"])
-        row["kv_bytes"] = ds.kv_bytes(wl.ctx)
-        row["step_bytes"] = footprint
-        row["kv_gbs"] = row["kv_bytes"] / (best * 1e-6) / 1e9
-        row["kv_frac_of_" + peak_kind] = row["kv_gbs"] / hbm_peak
-        if binding.pa_read_error_flags(reset=True):
-            raise RuntimeError("device error flags set")
-        print(json.dumps(row), flush=True)
-        del ds
-        torch.cuda.empty_cache()
+    return rows
 
 
 def run_profile(args, spec):

@@ -14,7 +14,10 @@
  * allocates memory: the caller owns every buffer, including the split-K scratch
  * (pa_decode_step_static_scratch uses a scratch array inside the library instead).
  * The metadata, producer, reducer and pa_decode_step(_window) launches are recorded
- * into CUDA graphs by this library's benchmark and tests.  When use_pdl is non-zero the
+ * into CUDA graphs by this library's benchmark and tests.  The library keeps
+ * per-device state for the life of the process (the device address of its error word,
+ * kernel attributes, pa_decode_step_static_scratch's array address): after a
+ * cudaDeviceReset, do not call it on that device again.  When use_pdl is non-zero the
  * kernel is launched with the programmatic-stream-serialisation attribute, so it
  * may start while the previous kernel in the stream finishes; each kernel waits
  * (griddepcontrol.wait) before it reads anything an earlier kernel wrote.
@@ -303,6 +306,11 @@ PA_API pa_status pa_decode_step(
  * lse -> h_lse).  Returns without synchronising: the host outputs are valid once the
  * stream has completed.  h_* should be page-locked (cudaHostAlloc / pinned) for the
  * copies to be asynchronous; pageable memory works but the copies then block the host.
+ * Packed layout: when req_pool_indices starts right after q's last byte and seq_lens
+ * right after req_pool_indices, on the host and on the device alike, the three inputs
+ * move in one copy; when lse starts right after out's last byte on both sides, the two
+ * outputs move in one copy (each copy has a fixed latency far above the transfer time
+ * of these few hundred KB).  Any other layout takes one copy per buffer.
  *   h_q    [bs, num_q_heads, head_dim] bf16     h_req_pool_indices, h_seq_lens [bs] int64
  *   h_out  [bs, num_q_heads, head_dim] bf16     h_lse [bs, num_q_heads] fp32 or NULL
  *                                               (NULL exactly when lse is NULL)
@@ -381,18 +389,23 @@ PA_API pa_status pa_decode_step_window(
  * device memory.  The pages have no counterpart to this call; it is an addition of
  * this library.
  *
- * Some callers cannot call cudaMalloc where they run a decode step: code running while
- * a CUDA graph is being captured (cudaMalloc synchronises the device, which capture
- * forbids), runtimes whose device memory is owned entirely by their own allocator or
- * fixed at start-up, and plain C hosts with no allocator of their own.  This call
- * takes the same arguments as pa_decode_step except the workspace: the split-K
- * scratch comes from an array of PA_STATIC_SCRATCH_BYTES compiled into the library.
- * Inputs and outputs are still the caller's.
+ * Some callers cannot call cudaMalloc where they run a decode step: runtimes whose
+ * device memory is owned entirely by their own allocator or fixed at start-up (a
+ * cudaMalloc behind the allocator's back takes memory it has already handed out, or
+ * fails), code on a latency-critical path where cudaMalloc's implicit device
+ * synchronisation is not acceptable, and plain C hosts that link this library but have
+ * no device allocator of their own.  This call takes the same arguments as
+ * pa_decode_step except the workspace: the split-K scratch comes from an array of
+ * PA_STATIC_SCRATCH_BYTES compiled into the library.  Inputs and outputs are still the
+ * caller's.
  *   - Every GPU that loads the library holds that array until the process exits.
  *   - A step whose scratch, pa_workspace_bytes(bs, num_q_heads, head_dim, S), exceeds
  *     PA_STATIC_SCRATCH_BYTES returns PA_ERR_SCRATCH_LIMIT and launches nothing.
- *   - The first call on a device looks up the array's device address; make it before
- *     any stream capture.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current) and keeps it for the life of the process;
+ *     make that first call before any stream capture.  A cudaDeviceReset destroys
+ *     the array together with the context, and the kept address then names nothing:
+ *     do not call the library on that device again afterwards.
  *   - All calls share the array and it keeps the last call's contents (nothing in it
  *     needs to start at zero).  Calls whose work overlaps on the GPU race on it: keep
  *     them in order on one stream.

@@ -12,6 +12,23 @@
 #include "pa_internal.h"
 
 namespace {
+// Last CUDA failure seen by an entry point on this host thread (pa_last_error_string).
+thread_local char g_last_error[256] = "no CUDA error";
+}  // namespace
+
+namespace pa {
+
+pa_status from_cuda(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return PA_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "%s [%s]: %s (%s)", where, g_fail_site,
+           cudaGetErrorString(e), cudaGetErrorName(e));
+  g_fail_site = "launch";
+  return PA_ERR_CUDA;
+}
+
+}  // namespace pa
+
+namespace {
 
 // Device-side error word.  Kernels receive its device address; host code fetches
 // that address once per device with cudaGetSymbolAddress.
@@ -56,16 +73,7 @@ int sm_count_of_current_device() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Last CUDA failure seen by an entry point on this host thread (pa_last_error_string).
-thread_local char g_last_error[256] = "no CUDA error";
-
-pa_status from_cuda(cudaError_t e, const char* where) {
-  if (e == cudaSuccess) return PA_OK;
-  snprintf(g_last_error, sizeof(g_last_error), "%s [%s]: %s (%s)", where, pa::g_fail_site,
-           cudaGetErrorString(e), cudaGetErrorName(e));
-  pa::g_fail_site = "launch";
-  return PA_ERR_CUDA;
-}
+using pa::from_cuda;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -123,6 +131,27 @@ pa_status check_attention(const void* q, const void* k_cache, const void* v_cach
   if (group != 1 && group != 2 && group != 4 && group != 8 && group != 16)
     return PA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_seq_pages) * page_size > INT32_MAX) return PA_ERR_INVALID;
+  return PA_OK;
+}
+
+// Limits of the producer that will run (the selected implementation, the query tile,
+// the window bounds), checked before any launch.  The decode-step entry points call it
+// before they enqueue the metadata kernel, so a step rejected here changes no output.
+pa_status check_producer(int group, bool multi, int32_t max_q_len, int32_t window,
+                         int32_t max_seq_pages, int32_t page_size) {
+  const bool use_fma = g_producer.load() == PA_PRODUCER_FMA;
+  if (multi) {
+    if (max_q_len < 1) return PA_ERR_INVALID;
+    if (use_fma || static_cast<int64_t>(group) * max_q_len > 16) return PA_ERR_UNSUPPORTED;
+  }
+  if (use_fma && group > 8) return PA_ERR_UNSUPPORTED;
+  if (window != 0) {
+    if (window < 0) return PA_ERR_INVALID;
+    if (use_fma) return PA_ERR_UNSUPPORTED;
+    // keeps every window bound the kernel forms within int32
+    if (static_cast<int64_t>(max_seq_pages) * page_size > (int64_t{1} << 29))
+      return PA_ERR_UNSUPPORTED;
+  }
   return PA_OK;
 }
 
@@ -239,19 +268,12 @@ pa_status decode_splitk_impl(const void* q, const void* k_cache, const void* v_c
     return PA_ERR_INVALID;
   const int group = num_q_heads / num_kv_heads;
   const bool use_fma = g_producer.load() == PA_PRODUCER_FMA;
-  if (cu_seqlens_q != nullptr) {
-    if (max_q_len < 1) return PA_ERR_INVALID;
-    if (use_fma || static_cast<int64_t>(group) * max_q_len > 16) return PA_ERR_UNSUPPORTED;
-  }
-  if (use_fma && group > 8) return PA_ERR_UNSUPPORTED;
+  st = check_producer(group, cu_seqlens_q != nullptr, max_q_len, window, max_seq_pages,
+                      page_size);
+  if (st != PA_OK) return st;
   const int32_t q_rows = cu_seqlens_q != nullptr ? max_q_len : 1;
   int32_t split_pages = max_seq_pages;  // pages the split partition spans
   if (window != 0) {
-    if (window < 0) return PA_ERR_INVALID;
-    if (use_fma) return PA_ERR_UNSUPPORTED;
-    // keeps every window bound the kernel forms within int32
-    if (static_cast<int64_t>(max_seq_pages) * page_size > (int64_t{1} << 29))
-      return PA_ERR_UNSUPPORTED;
     const int64_t longest = static_cast<int64_t>(max_seq_pages) * page_size + q_rows;
     if (window > longest) window = static_cast<int32_t>(longest);  // same positions
     split_pages = pa_window_pages(window, q_rows, page_size, max_seq_pages);
@@ -460,6 +482,8 @@ pa_status decode_step_impl(
   if (!out || !workspace || !aligned16(workspace)) return PA_ERR_INVALID;
   if (workspace_bytes < pa_workspace_bytes(bs, num_q_heads, head_dim, splits))
     return PA_ERR_INVALID;
+  st = check_producer(num_q_heads / num_kv_heads, false, 1, window, max_seq_pages, page_size);
+  if (st != PA_OK) return st;
   const size_t rows = static_cast<size_t>(bs) * num_q_heads * splits;
   char* ws = static_cast<char*>(workspace);
   float* m = reinterpret_cast<float*>(ws);
@@ -527,13 +551,29 @@ pa_status pa_decode_step_host(
   const size_t rows = static_cast<size_t>(bs) * num_q_heads;
   const size_t qo_bytes = rows * static_cast<size_t>(head_dim) * 2;
   const size_t idx_bytes = static_cast<size_t>(bs) * sizeof(int64_t);
-  cudaError_t e = cudaMemcpyAsync(const_cast<void*>(q), h_q, qo_bytes, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(const_cast<int64_t*>(req_pool_indices), h_req_pool_indices, idx_bytes,
+  // Each copy costs a fixed latency far above its transfer time at these sizes, so
+  // buffers laid out back to back (q, req_pool_indices, seq_lens on both sides; out,
+  // lse on both sides) move in one copy each.
+  const char* hq = static_cast<const char*>(h_q);
+  const char* dq = static_cast<const char*>(q);
+  const bool inputs_packed =
+      reinterpret_cast<const char*>(h_req_pool_indices) == hq + qo_bytes &&
+      reinterpret_cast<const char*>(h_seq_lens) == hq + qo_bytes + idx_bytes &&
+      reinterpret_cast<const char*>(req_pool_indices) == dq + qo_bytes &&
+      reinterpret_cast<const char*>(seq_lens) == dq + qo_bytes + idx_bytes;
+  cudaError_t e = cudaSuccess;
+  if (inputs_packed) {
+    e = cudaMemcpyAsync(const_cast<void*>(q), h_q, qo_bytes + 2 * idx_bytes,
                         cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(const_cast<int64_t*>(seq_lens), h_seq_lens, idx_bytes,
-                        cudaMemcpyHostToDevice, s);
+  } else {
+    e = cudaMemcpyAsync(const_cast<void*>(q), h_q, qo_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<int64_t*>(req_pool_indices), h_req_pool_indices,
+                          idx_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<int64_t*>(seq_lens), h_seq_lens, idx_bytes,
+                          cudaMemcpyHostToDevice, s);
+  }
   if (e != cudaSuccess) return from_cuda(e, "host-to-device input copy");
   pa_status st = decode_step_impl(
       req_pool_indices, seq_lens, req_to_token, req_to_token_rows, req_to_token_stride,
@@ -543,9 +583,16 @@ pa_status pa_decode_step_host(
       page_size, num_pages, 0, num_splits, sm_scale, workspace, workspace_bytes, out, lse, stream,
       use_pdl);
   if (st != PA_OK) return st;
-  e = cudaMemcpyAsync(h_out, out, qo_bytes, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess && h_lse != nullptr)
-    e = cudaMemcpyAsync(h_lse, lse, rows * sizeof(float), cudaMemcpyDeviceToHost, s);
+  const bool outputs_packed =
+      h_lse != nullptr && reinterpret_cast<char*>(h_lse) == static_cast<char*>(h_out) + qo_bytes &&
+      reinterpret_cast<char*>(lse) == static_cast<char*>(out) + qo_bytes;
+  if (outputs_packed) {
+    e = cudaMemcpyAsync(h_out, out, qo_bytes + rows * sizeof(float), cudaMemcpyDeviceToHost, s);
+  } else {
+    e = cudaMemcpyAsync(h_out, out, qo_bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && h_lse != nullptr)
+      e = cudaMemcpyAsync(h_lse, lse, rows * sizeof(float), cudaMemcpyDeviceToHost, s);
+  }
   return from_cuda(e, "device-to-host output copy");
 }
 
@@ -568,9 +615,9 @@ pa_status pa_decode_step_multi(
   if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
     return PA_ERR_INVALID;
   // the multi-query producer's limits, before anything is enqueued
-  if (g_producer.load() == PA_PRODUCER_FMA ||
-      static_cast<int64_t>(num_q_heads / num_kv_heads) * max_q_len > 16)
-    return PA_ERR_UNSUPPORTED;
+  pa_status st = check_producer(num_q_heads / num_kv_heads, true, max_q_len, 0, max_seq_pages,
+                                page_size);
+  if (st != PA_OK) return st;
   const int32_t splits =
       num_splits > 0 ? num_splits
                      : pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, kv_dtype, 0);
@@ -580,7 +627,7 @@ pa_status pa_decode_step_multi(
       return PA_ERR_INVALID;
   }
   // the attention arguments are checked before anything is enqueued
-  pa_status st = check_attention(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
+  st = check_attention(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, page_table,
                                  page_table_stride, cache_seqlens, bs, num_q_heads,
                                  num_kv_heads, head_dim, page_size, num_pages, max_seq_pages,
                                  splits);

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/pa.h"
+
 namespace pa {
 
 struct MetadataParams {
@@ -90,6 +92,10 @@ inline cudaError_t fail_at(cudaError_t e, const char* site) {
   if (e != cudaSuccess) g_fail_site = site;
   return e;
 }
+
+// PA_OK for cudaSuccess; otherwise records `where`, the failed step and the CUDA error
+// for pa_last_error_string on this host thread and returns PA_ERR_CUDA.
+pa_status from_cuda(cudaError_t e, const char* where);
 
 cudaError_t launch_metadata(const MetadataParams& p, cudaStream_t stream, bool use_pdl);
 

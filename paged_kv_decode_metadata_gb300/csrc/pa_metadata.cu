@@ -8,11 +8,15 @@
 //
 // Grid: blocks [0, bs) each own one request row (its cache_seqlens entry and its
 // page-table row(s)); block bs runs the in-block scans; blocks after it translate
-// swa_out_cache_loc in tiles of kThreads entries.  Every block waits on the previous
-// grid before its first global access (so a PDL launch never overwrites a page
-// table that a previous step's producer may still read) and triggers its dependents
-// straight after: the producer reads nothing this kernel reads, and its own
-// griddepcontrol.wait blocks until this grid has completed and flushed.
+// swa_out_cache_loc in tiles of kThreads entries.  Every block triggers its
+// dependents on entry, so the producer's blocks become resident and load Q while
+// this grid still runs: the producer reads nothing of this kernel's outputs before
+// its own griddepcontrol.wait, which blocks until this grid has completed and
+// flushed.  Then every block waits on the previous grid before its first global
+// access, so a PDL launch never overwrites a page table that a previous step's
+// producer may still read.  (All of this grid's blocks are resident before the
+// producer can launch, since a grid triggers only once every block has issued the
+// trigger; the early producer blocks cannot hold SMs this grid still needs.)
 #include <utility>
 
 #include "pa_common.cuh"
@@ -59,9 +63,9 @@ __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* w
 
 __global__ void __launch_bounds__(kThreads) metadata_kernel(const MetadataParams p) {
   PA_TS_FIRST(p.ts, 0, kTsEntry);
+  trigger_dependents();
   grid_dependency_wait();
   PA_TS_FIRST(p.ts, 0, kTsReady);
-  trigger_dependents();
 
   const int tid = threadIdx.x;
   const int blk = blockIdx.x;

@@ -89,7 +89,7 @@ struct Layout {
   static constexpr int OFF_FULL = OFF_PAGES + kMaxSplitPages * 4;
   static constexpr int OFF_EMPTY = OFF_FULL + STAGES * 8;
   static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;      // [4 warps][16 columns][3]
-  static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 3 * 4;    // abort flag
+  static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 3 * 4;  // abort, issued, done
   static constexpr int OFF_SKIP = OFF_MISC + 16;  // per stage: mask of its skipped pages
   static constexpr int SMEM = OFF_SKIP + (STAGES * 4 + 15) / 16 * 16 + 1024;  // + alignment slack
   static constexpr int RED_BYTES = kConsumerWarps * 16 * 128 * 4;           // output merge buffer
@@ -268,7 +268,20 @@ __global__ void __launch_bounds__(kThreads, MINB)
   int32_t* pages_s = reinterpret_cast<int32_t*>(smem + L::OFF_PAGES);
   float* ml_s = reinterpret_cast<float*>(smem + L::OFF_ML);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC);
+  // chunks the TMA warp has issued (or skipped), and whether it has stopped issuing:
+  // the failure path drains exactly the copies that were issued
+  volatile int* issued_s = abort_flag + 1;
+  volatile int* producer_done = abort_flag + 2;
   uint32_t* skip_s = reinterpret_cast<uint32_t*>(smem + L::OFF_SKIP);
+  // Wait (bounded) for the copies of the first `issued` chunks to land: per stage, the
+  // phase of its last issued chunk (earlier phases of that stage completed before the
+  // stage was refilled, so that phase is the only one that can be pending).
+  auto drain_issued = [&](int issued) {
+    for (int st = 0; st < STAGES && st < issued; ++st) {
+      const int last = st + (issued - 1 - st) / STAGES * STAGES;
+      if (!mbar_wait_bounded(&full[st], static_cast<uint32_t>(last / STAGES) & 1u)) break;
+    }
+  };
 
   // ---- prologue independent of the metadata stage: Q^T fragments in registers ------
   // (with several queries per request their rows come from cu_seqlens_q, a metadata
@@ -284,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
       mbar_init(&empty[s], kConsumerWarps);
     }
     *abort_flag = 0;
+    *issued_s = 0;
+    *producer_done = 0;
     fence_barrier_init();
   }
 
@@ -354,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // failure-detection test of the instrumented build: nothing is issued, so every
     // consumer wait gives up after its time limit and the kernel reports it
     if (prm.hold_loads) {
+      if (lane == 0) *producer_done = 1;
       trigger_dependents();
       return;
     }
@@ -370,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             break;
           }
         }
+        *issued_s = c + 1;
         const uint32_t kdst = smem_base + stage * L::STAGE_BYTES;
         const uint32_t vdst = kdst + L::KV_BYTES;
         const int ctok = c * kChunk;
@@ -459,6 +476,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
           }
         }
       }
+      // stopped early: the consumers have given up, so nothing else waits for these
+      if (*abort_flag) drain_issued(*issued_s);
+      __threadfence_block();
+      *producer_done = 1;
     }
     trigger_dependents();
     return;
@@ -769,10 +790,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
   }
   consumer_barrier();
   if (failed || *abort_flag) {
-    // Drain what the producer issued so no TMA write lands after the CTA exits.
+    // Drain what the TMA warp issued so no copy lands after the CTA exits.  It may
+    // first sit out its own bounded wait on a stage the consumers never released.
     if (tid == 0) {
-      for (int c = 0; c < n_chunks; ++c) {
-        if (!mbar_wait_bounded(&full[c % STAGES], static_cast<uint32_t>(c / STAGES) & 1u)) break;
+      const unsigned long long start = global_timer_ns();
+      while (*producer_done == 0 && global_timer_ns() - start < 2 * kWaitLimitNs) {
+      }
+      if (*producer_done != 0) {
+        __threadfence_block();
+        drain_issued(*issued_s);
       }
     }
     return;

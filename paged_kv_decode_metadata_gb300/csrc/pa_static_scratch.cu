@@ -2,11 +2,12 @@
 // a fixed array compiled into this library instead of a caller-provided workspace.
 //
 // It exists for callers that cannot allocate device memory at the point where they
-// run a decode step: code that runs while a CUDA graph is being captured (cudaMalloc
-// synchronises the device, which a capture does not allow), runtimes whose device
-// memory is handed out entirely by their own allocator or fixed at start-up, and
-// plain C hosts that link this library but have no allocator of their own.  Such a
-// caller still passes its inputs and outputs; only the scratch moves here.
+// run a decode step: runtimes whose device memory is handed out entirely by their own
+// allocator or fixed at start-up (a cudaMalloc behind the allocator's back takes memory
+// it has already promised, or fails), code on a latency-critical path where cudaMalloc's
+// implicit device synchronisation is not acceptable, and plain C hosts that link this
+// library but have no device allocator of their own.  Such a caller still passes its
+// inputs and outputs; only the scratch moves here.
 //
 // Costs and rules:
 //   * Every GPU that loads the library holds PA_STATIC_SCRATCH_BYTES for the array
@@ -17,7 +18,9 @@
 //     (different streams, or graphs replayed concurrently) race on the array and give
 //     wrong results; order them on one stream.
 //   * The first call on a device looks up the array's device address (once per device,
-//     with that device current).  Make that first call before any stream capture.
+//     with that device current) and keeps it for the life of the process.  Make that
+//     first call before any stream capture.  After a cudaDeviceReset the kept address
+//     names nothing: the library must not be called on that device again.
 //   * A step that needs more scratch than the array holds is rejected with
 //     PA_ERR_SCRATCH_LIMIT before anything is launched.
 //   * Nothing here allocates: no cudaMalloc, no cudaFree, no allocating library call.
@@ -26,6 +29,7 @@
 #include <atomic>
 
 #include "../../include/pa.h"
+#include "pa_internal.h"
 
 namespace {
 
@@ -75,7 +79,8 @@ extern "C" pa_status pa_decode_step_static_scratch(
   if (need == 0) return PA_ERR_INVALID;
   if (need > PA_STATIC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
-  if (static_scratch_address(&scratch) != cudaSuccess) return PA_ERR_CUDA;
+  const cudaError_t e = static_scratch_address(&scratch);
+  if (e != cudaSuccess) return pa::from_cuda(e, "static scratch address");
   return pa_decode_step(req_pool_indices, seq_lens, req_to_token, req_to_token_rows,
                         req_to_token_stride, full_to_swa_mapping, full_to_swa_mapping_len,
                         seqlen_offset, max_seq_pages, cache_seqlens, cu_seqlens_k, page_table,

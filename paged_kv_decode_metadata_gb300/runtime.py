@@ -27,10 +27,14 @@ class DeviceStep:
         self.max_seq_pages = wl.max_seq_pages
         self.sm_scale = wl.sm_scale
         to = dict(device=device)
-        self.req_pool_indices = wl.req_pool_indices.to(**to)
-        self.seq_lens = wl.seq_lens.to(**to)
+        # q, req_pool_indices and seq_lens back to back in one buffer (and out, lse in
+        # another): pa_decode_step_host then moves each group with one copy
+        self._inputs = torch.empty(self._input_bytes(), dtype=torch.uint8, device=device)
+        self.q, self.req_pool_indices, self.seq_lens = self._input_views(self._inputs)
+        self.q.copy_(wl.q)
+        self.req_pool_indices.copy_(wl.req_pool_indices)
+        self.seq_lens.copy_(wl.seq_lens)
         self.req_to_token = wl.req_to_token.to(**to)
-        self.q = wl.q.to(**to)
         # (a workload drawn without its full pool leaves these None)
         self.k_cache = wl.k_cache.to(**to) if wl.k_cache is not None else None
         self.v_cache = wl.v_cache.to(**to) if wl.v_cache is not None else None
@@ -58,10 +62,43 @@ class DeviceStep:
         self.workspace = torch.empty(
             B.pa_workspace_bytes(self.bs, self.num_q_heads, self.head_dim, S),
             dtype=torch.uint8, device=device)
-        self.out = torch.empty((self.bs, self.num_q_heads, self.head_dim), dtype=torch.bfloat16,
-                               device=device)
-        self.lse = torch.empty((self.bs, self.num_q_heads), **f32)
+        self._outputs = torch.empty(self._output_bytes(), dtype=torch.uint8, device=device)
+        self.out, self.lse = self._output_views(self._outputs)
         self._prepared = {}
+
+    # ---- packed input / output groups ----------------------------------------------
+    def _q_bytes(self):
+        return self.bs * self.num_q_heads * self.head_dim * 2
+
+    def _input_bytes(self):
+        return self._q_bytes() + 2 * self.bs * 8
+
+    def _output_bytes(self):
+        return self._q_bytes() + self.bs * self.num_q_heads * 4
+
+    def _input_views(self, buf):
+        """q [bs, Hq, d] bf16, req_pool_indices [bs] int64, seq_lens [bs] int64, back to
+        back in ``buf``."""
+        qb = self._q_bytes()
+        q = buf[:qb].view(torch.bfloat16).view(self.bs, self.num_q_heads, self.head_dim)
+        rpi = buf[qb:qb + 8 * self.bs].view(torch.int64)
+        sl = buf[qb + 8 * self.bs:qb + 16 * self.bs].view(torch.int64)
+        return q, rpi, sl
+
+    def _output_views(self, buf):
+        """out [bs, Hq, d] bf16 and lse [bs, Hq] fp32, back to back in ``buf``."""
+        qb = self._q_bytes()
+        out = buf[:qb].view(torch.bfloat16).view(self.bs, self.num_q_heads, self.head_dim)
+        lse = buf[qb:].view(torch.float32).view(self.bs, self.num_q_heads)
+        return out, lse
+
+    def host_buffers(self):
+        """Pinned host buffers laid out like this step's device input and output groups:
+        (h_q, h_req_pool_indices, h_seq_lens, h_out, h_lse) for ``prepare_host_step``,
+        which then needs one copy in and one copy out per step."""
+        h_in = torch.empty(self._input_bytes(), dtype=torch.uint8, pin_memory=True)
+        h_outs = torch.empty(self._output_bytes(), dtype=torch.uint8, pin_memory=True)
+        return (*self._input_views(h_in), *self._output_views(h_outs))
 
     # ---- the three stages ---------------------------------------------------------
     def metadata(self, use_pdl=True, stream=None):

@@ -24,3 +24,10 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    # per-band attention errors of every parity check, when PA_PARITY_REPORT names a file
+    helpers = sys.modules.get("helpers")
+    if helpers is not None:
+        helpers.write_parity_report()

@@ -10,7 +10,7 @@ from paged_kv_decode_metadata_gb300 import binding as B
 from paged_kv_decode_metadata_gb300 import build, synthetic
 from paged_kv_decode_metadata_gb300.runtime import DeviceStep
 
-from helpers import assert_attention_close, bits, kv_np, oracle_metadata
+from helpers import Expected, assert_attention_close, bits, kv_np, oracle_metadata
 
 pytestmark = pytest.mark.gpu
 
@@ -62,8 +62,8 @@ def _oracle_multi(wl, qlens, q):
     meta = oracle_metadata(wl)
     k, v, ks, vs = kv_np(wl)
     cu_q = oracle.cu_seqlens_q(qlens.numpy(), wl.spec.bs, 1)
-    return oracle.paged_attention_multi(bits(q), k, v, meta["page_table"], meta["cache_seqlens"],
-                                        cu_q, wl.sm_scale, ks, vs)
+    return Expected(oracle.paged_attention_multi, bits(q), k, v, meta["page_table"],
+                    meta["cache_seqlens"], cu_q, wl.sm_scale, ks, vs)
 
 
 CASES = [  # seed, kv, group, max_q_len, page_size, splits
@@ -82,8 +82,7 @@ def test_multi_query_matches_oracle(seed, kv, grp, max_q, P, splits):
     qlens = synthetic.draw_query_lengths(spec.bs, max_q, 800 + seed)
     q = synthetic.draw_queries(int(qlens.sum()), spec.num_q_heads, spec.head_dim, 900 + seed)
     out, lse = _run_multi(wl, qlens, q, splits)
-    out_ref, lse_ref = _oracle_multi(wl, qlens, q)
-    assert_attention_close(out, lse, out_ref, lse_ref, spec.name)
+    assert_attention_close(out, lse, _oracle_multi(wl, qlens, q), spec.name)
 
 
 def test_queries_beyond_the_context_are_empty():
@@ -93,9 +92,9 @@ def test_queries_beyond_the_context_are_empty():
     qlens = torch.tensor([4, 4, 4], dtype=torch.int64)   # more queries than cached tokens
     q = synthetic.draw_queries(12, 8, 128, 32)
     out, lse = _run_multi(wl, qlens, q, 2)
-    out_ref, lse_ref = _oracle_multi(wl, qlens, q)
-    assert np.isneginf(lse_ref).any()
-    assert_attention_close(out, lse, out_ref, lse_ref, "short")
+    ref = _oracle_multi(wl, qlens, q)
+    assert np.isneginf(ref.lse).any()
+    assert_attention_close(out, lse, ref, "short")
 
 
 def test_one_query_per_request_equals_decode_bit_for_bit():
@@ -164,5 +163,4 @@ def test_multi_step_one_call_matches_stages(q_mode):
                            q_stride=3)
     torch.cuda.synchronize()
     assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
-    o2, l2 = _oracle_multi(wl, qlens, q)
-    assert_attention_close(out, lse, o2, l2, f"step multi {q_mode}")
+    assert_attention_close(out, lse, _oracle_multi(wl, qlens, q), f"step multi {q_mode}")
