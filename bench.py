@@ -589,15 +589,14 @@ def producer_bytes(ds, wl, pages_read):
 
 
 def e2e_us(torch, ds, stream, n):
-    """End to end through pa_decode_step_host: pinned host inputs copied in, the three
-    kernels, outputs copied back, then a stream sync, n times; returns (us per step,
-    h2d bytes, d2h bytes).  The host buffers are laid out like the device groups, so a
-    step makes one copy each way."""
-    h_q, h_rpi, h_sl, h_out, h_lse = ds.host_buffers()
+    """End to end through pa_decode_step_host_packed: pinned host inputs copied in (one
+    copy), the three kernels, outputs copied back (one copy), then a stream sync, n
+    times; returns (us per step, h2d bytes, d2h bytes)."""
+    h_in, h_outs, (h_q, h_rpi, h_sl, h_out, h_lse) = ds.host_buffers()
     h_q.copy_(ds.q)
     h_rpi.copy_(ds.req_pool_indices)
     h_sl.copy_(ds.seq_lens)
-    host_step = ds.prepare_host_step(h_q, h_rpi, h_sl, h_out, h_lse, use_pdl=True, stream=stream)
+    host_step = ds.prepare_packed_host_step(h_in, h_outs, use_pdl=True, stream=stream)
     for _ in range(20):
         host_step()
         stream.synchronize()

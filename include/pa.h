@@ -306,11 +306,7 @@ PA_API pa_status pa_decode_step(
  * lse -> h_lse).  Returns without synchronising: the host outputs are valid once the
  * stream has completed.  h_* should be page-locked (cudaHostAlloc / pinned) for the
  * copies to be asynchronous; pageable memory works but the copies then block the host.
- * Packed layout: when req_pool_indices starts right after q's last byte and seq_lens
- * right after req_pool_indices, on the host and on the device alike, the three inputs
- * move in one copy; when lse starts right after out's last byte on both sides, the two
- * outputs move in one copy (each copy has a fixed latency far above the transfer time
- * of these few hundred KB).  Any other layout takes one copy per buffer.
+ * (pa_decode_step_host_packed does the same with one copy each way.)
  *   h_q    [bs, num_q_heads, head_dim] bf16     h_req_pool_indices, h_seq_lens [bs] int64
  *   h_out  [bs, num_q_heads, head_dim] bf16     h_lse [bs, num_q_heads] fp32 or NULL
  *                                               (NULL exactly when lse is NULL)
@@ -330,6 +326,37 @@ PA_API pa_status pa_decode_step_host(
     int32_t head_dim, int32_t page_size, int64_t num_pages, int32_t num_splits,
     float sm_scale, void* workspace, size_t workspace_bytes, void* out, float* lse,
     void* stream, int32_t use_pdl);
+
+/*
+ * pa_decode_step_host_packed -- pa_decode_step_host with the per-step inputs in one
+ * buffer and the outputs in another, so a step makes one host-to-device and one
+ * device-to-host copy (each copy has a fixed latency well above the transfer time of
+ * these few hundred KB).  Layout, the same in host and device memory:
+ *   inputs   q [bs, num_q_heads, head_dim] bf16, then req_pool_indices [bs] int64,
+ *            then seq_lens [bs] int64, back to back: pa_packed_input_bytes() bytes
+ *   outputs  out [bs, num_q_heads, head_dim] bf16, then lse [bs, num_q_heads] fp32,
+ *            back to back: pa_packed_output_bytes() bytes
+ * h_inputs / h_outputs are one host allocation each (page-locked for asynchronous
+ * copies); inputs / outputs one device allocation each, 16-byte aligned.  Enqueued on
+ * `stream`: h_inputs -> inputs, the three kernels of pa_decode_step reading q,
+ * req_pool_indices and seq_lens from `inputs` and writing out and lse into `outputs`,
+ * outputs -> h_outputs.  The remaining arguments are those of pa_decode_step.  Errors:
+ * PA_ERR_INVALID for a NULL or misaligned buffer, and as pa_decode_step; a failed copy
+ * returns PA_ERR_CUDA.
+ */
+PA_API size_t pa_packed_input_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim);
+PA_API size_t pa_packed_output_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim);
+PA_API pa_status pa_decode_step_host_packed(
+    const void* h_inputs, void* inputs, void* h_outputs, void* outputs,
+    const int32_t* req_to_token, int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const void* k_cache,
+    const void* v_cache, const float* k_scale, const float* v_scale, int32_t kv_dtype,
+    int32_t bs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+    int64_t num_pages, int32_t num_splits, float sm_scale, void* workspace,
+    size_t workspace_bytes, void* stream, int32_t use_pdl);
 
 /*
  * pa_decode_step_multi -- the decode step for several query tokens per request

@@ -105,6 +105,13 @@ def _declare(lib):
                                    vp, i64, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                    i64, i32, f32, vp, sz, vp, vp, vp, i32]
     lib.pa_decode_step_host.argtypes = [vp, vp, vp, vp, vp] + lib.pa_decode_step.argtypes
+    step = lib.pa_decode_step.argtypes
+    lib.pa_decode_step_host_packed.argtypes = [vp, vp, vp, vp] + step[2:15] + step[16:31] + \
+        step[33:35]
+    lib.pa_packed_input_bytes.argtypes = [i32, i32, i32]
+    lib.pa_packed_input_bytes.restype = sz
+    lib.pa_packed_output_bytes.argtypes = [i32, i32, i32]
+    lib.pa_packed_output_bytes.restype = sz
     lib.pa_decode_step_multi.argtypes = [vp, vp, vp, i64, i64, vp, i64, i32, i32, vp, vp, vp,
                                          i64, vp, i64, vp, i32, i32, vp, vp, i32, i32, vp, vp,
                                          vp, vp, i32, i32, i32, i32, i32, i32, i64, i32, f32, vp,
@@ -130,7 +137,8 @@ def _declare(lib):
     lib.pa_read_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     for name in ("pa_build_metadata", "pa_build_metadata_full", "pa_decode_splitk",
                  "pa_decode_splitk_multi", "pa_decode_splitk_window", "pa_reduce",
-                 "pa_decode_step", "pa_decode_step_host", "pa_decode_step_multi",
+                 "pa_decode_step", "pa_decode_step_host", "pa_decode_step_host_packed",
+                 "pa_decode_step_multi",
                  "pa_decode_step_window",
                  "pa_read_error_flags"):
         getattr(lib, name).restype = ctypes.c_int
@@ -389,6 +397,29 @@ def pa_decode_step_host(*, lib=None, **kw):
     _check("pa_decode_step_host", lib.pa_decode_step_host(*_decode_step_host_args(**kw)), lib)
 
 
+def _decode_step_host_packed_args(*, h_inputs, inputs, h_outputs, outputs, **kw):
+    """``kw``: the arguments of ``pa_decode_step``, whose q, req_pool_indices and
+    seq_lens must be the views of ``inputs``, and out and lse those of ``outputs``, that
+    the packed layout defines (their pointers are not passed; only shapes are read)."""
+    a = _decode_step_args(**kw)
+    bs, hq, d = a[21], a[22], a[24]
+    lib = load()
+    for t, name, n in ((h_inputs, "h_inputs", lib.pa_packed_input_bytes(bs, hq, d)),
+                       (h_outputs, "h_outputs", lib.pa_packed_output_bytes(bs, hq, d))):
+        if t.is_cuda or not t.is_contiguous() or t.numel() * t.element_size() < n:
+            raise ValueError(f"{name} must be a contiguous host buffer of {n} bytes")
+    for t, name, n in ((inputs, "inputs", lib.pa_packed_input_bytes(bs, hq, d)),
+                       (outputs, "outputs", lib.pa_packed_output_bytes(bs, hq, d))):
+        if not t.is_cuda or not t.is_contiguous() or t.numel() * t.element_size() < n:
+            raise ValueError(f"{name} must be a contiguous device buffer of {n} bytes")
+    if a[15] != inputs.data_ptr() or a[0] != inputs.data_ptr() + d * hq * bs * 2 or \
+            a[31] != outputs.data_ptr() or (a[32] is not None and
+                                            a[32] != outputs.data_ptr() + d * hq * bs * 2):
+        raise ValueError("q / req_pool_indices / seq_lens and out / lse must be the packed views")
+    return (h_inputs.data_ptr(), inputs.data_ptr(), h_outputs.data_ptr(),
+            outputs.data_ptr()) + a[2:15] + a[16:31] + a[33:35]
+
+
 def pa_decode_step_multi(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset: int,
                          max_seq_pages: int, cache_seqlens, cu_seqlens_k, page_table,
                          cu_seqlens_q, q, max_q_len: int, k_cache, v_cache, num_splits: int,
@@ -484,6 +515,11 @@ def prepare_decode_step(*, lib=None, **kw) -> PreparedCall:
 def prepare_decode_step_host(*, lib=None, **kw) -> PreparedCall:
     """``pa_decode_step_host`` with the given keyword arguments, marshalled once."""
     return PreparedCall("pa_decode_step_host", _decode_step_host_args(**kw), lib)
+
+
+def prepare_decode_step_host_packed(*, lib=None, **kw) -> PreparedCall:
+    """``pa_decode_step_host_packed`` with the given keyword arguments, marshalled once."""
+    return PreparedCall("pa_decode_step_host_packed", _decode_step_host_packed_args(**kw), lib)
 
 
 def prepare_decode_step_window(*, lib=None, **kw) -> PreparedCall:

@@ -551,29 +551,13 @@ pa_status pa_decode_step_host(
   const size_t rows = static_cast<size_t>(bs) * num_q_heads;
   const size_t qo_bytes = rows * static_cast<size_t>(head_dim) * 2;
   const size_t idx_bytes = static_cast<size_t>(bs) * sizeof(int64_t);
-  // Each copy costs a fixed latency far above its transfer time at these sizes, so
-  // buffers laid out back to back (q, req_pool_indices, seq_lens on both sides; out,
-  // lse on both sides) move in one copy each.
-  const char* hq = static_cast<const char*>(h_q);
-  const char* dq = static_cast<const char*>(q);
-  const bool inputs_packed =
-      reinterpret_cast<const char*>(h_req_pool_indices) == hq + qo_bytes &&
-      reinterpret_cast<const char*>(h_seq_lens) == hq + qo_bytes + idx_bytes &&
-      reinterpret_cast<const char*>(req_pool_indices) == dq + qo_bytes &&
-      reinterpret_cast<const char*>(seq_lens) == dq + qo_bytes + idx_bytes;
-  cudaError_t e = cudaSuccess;
-  if (inputs_packed) {
-    e = cudaMemcpyAsync(const_cast<void*>(q), h_q, qo_bytes + 2 * idx_bytes,
+  cudaError_t e = cudaMemcpyAsync(const_cast<void*>(q), h_q, qo_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<int64_t*>(req_pool_indices), h_req_pool_indices, idx_bytes,
                         cudaMemcpyHostToDevice, s);
-  } else {
-    e = cudaMemcpyAsync(const_cast<void*>(q), h_q, qo_bytes, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(const_cast<int64_t*>(req_pool_indices), h_req_pool_indices,
-                          idx_bytes, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(const_cast<int64_t*>(seq_lens), h_seq_lens, idx_bytes,
-                          cudaMemcpyHostToDevice, s);
-  }
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(const_cast<int64_t*>(seq_lens), h_seq_lens, idx_bytes,
+                        cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return from_cuda(e, "host-to-device input copy");
   pa_status st = decode_step_impl(
       req_pool_indices, seq_lens, req_to_token, req_to_token_rows, req_to_token_stride,
@@ -583,16 +567,56 @@ pa_status pa_decode_step_host(
       page_size, num_pages, 0, num_splits, sm_scale, workspace, workspace_bytes, out, lse, stream,
       use_pdl);
   if (st != PA_OK) return st;
-  const bool outputs_packed =
-      h_lse != nullptr && reinterpret_cast<char*>(h_lse) == static_cast<char*>(h_out) + qo_bytes &&
-      reinterpret_cast<char*>(lse) == static_cast<char*>(out) + qo_bytes;
-  if (outputs_packed) {
-    e = cudaMemcpyAsync(h_out, out, qo_bytes + rows * sizeof(float), cudaMemcpyDeviceToHost, s);
-  } else {
-    e = cudaMemcpyAsync(h_out, out, qo_bytes, cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess && h_lse != nullptr)
-      e = cudaMemcpyAsync(h_lse, lse, rows * sizeof(float), cudaMemcpyDeviceToHost, s);
-  }
+  e = cudaMemcpyAsync(h_out, out, qo_bytes, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && h_lse != nullptr)
+    e = cudaMemcpyAsync(h_lse, lse, rows * sizeof(float), cudaMemcpyDeviceToHost, s);
+  return from_cuda(e, "device-to-host output copy");
+}
+
+size_t pa_packed_input_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim) {
+  if (bs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+  return static_cast<size_t>(bs) * num_q_heads * head_dim * 2 + 2 * sizeof(int64_t) * bs;
+}
+
+size_t pa_packed_output_bytes(int32_t bs, int32_t num_q_heads, int32_t head_dim) {
+  if (bs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+  return static_cast<size_t>(bs) * num_q_heads * (head_dim * 2 + sizeof(float));
+}
+
+pa_status pa_decode_step_host_packed(
+    const void* h_inputs, void* inputs, void* h_outputs, void* outputs,
+    const int32_t* req_to_token, int64_t req_to_token_rows, int64_t req_to_token_stride,
+    const int64_t* full_to_swa_mapping, int64_t full_to_swa_mapping_len,
+    int32_t seqlen_offset, int32_t max_seq_pages, int32_t* cache_seqlens,
+    int32_t* cu_seqlens_k, int32_t* page_table, int64_t page_table_stride,
+    int32_t* swa_page_table, int64_t swa_page_table_stride, const void* k_cache,
+    const void* v_cache, const float* k_scale, const float* v_scale, int32_t kv_dtype,
+    int32_t bs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+    int64_t num_pages, int32_t num_splits, float sm_scale, void* workspace,
+    size_t workspace_bytes, void* stream, int32_t use_pdl) {
+  if (bs < 0 || num_q_heads < 1 || head_dim < 1) return PA_ERR_INVALID;
+  if (bs == 0) return PA_OK;
+  if (!h_inputs || !inputs || !h_outputs || !outputs) return PA_ERR_INVALID;
+  if (!aligned16(inputs) || !aligned16(outputs)) return PA_ERR_INVALID;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t qo_bytes = static_cast<size_t>(bs) * num_q_heads * head_dim * 2;
+  char* in = static_cast<char*>(inputs);
+  char* outs = static_cast<char*>(outputs);
+  const int64_t* rpi = reinterpret_cast<const int64_t*>(in + qo_bytes);
+  const int64_t* sl = rpi + bs;
+  float* lse = reinterpret_cast<float*>(outs + qo_bytes);
+  cudaError_t e = cudaMemcpyAsync(inputs, h_inputs, pa_packed_input_bytes(bs, num_q_heads, head_dim),
+                                  cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return from_cuda(e, "host-to-device input copy");
+  pa_status st = decode_step_impl(
+      rpi, sl, req_to_token, req_to_token_rows, req_to_token_stride, full_to_swa_mapping,
+      full_to_swa_mapping_len, seqlen_offset, max_seq_pages, cache_seqlens, cu_seqlens_k,
+      page_table, page_table_stride, swa_page_table, swa_page_table_stride, in, k_cache, v_cache,
+      k_scale, v_scale, kv_dtype, bs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+      0, num_splits, sm_scale, workspace, workspace_bytes, outs, lse, stream, use_pdl);
+  if (st != PA_OK) return st;
+  e = cudaMemcpyAsync(h_outputs, outputs, pa_packed_output_bytes(bs, num_q_heads, head_dim),
+                      cudaMemcpyDeviceToHost, s);
   return from_cuda(e, "device-to-host output copy");
 }
 

@@ -27,8 +27,8 @@ class DeviceStep:
         self.max_seq_pages = wl.max_seq_pages
         self.sm_scale = wl.sm_scale
         to = dict(device=device)
-        # q, req_pool_indices and seq_lens back to back in one buffer (and out, lse in
-        # another): pa_decode_step_host then moves each group with one copy
+        # q, req_pool_indices and seq_lens back to back in one buffer, out and lse in
+        # another: the packed layout of pa_decode_step_host_packed (one copy each way)
         self._inputs = torch.empty(self._input_bytes(), dtype=torch.uint8, device=device)
         self.q, self.req_pool_indices, self.seq_lens = self._input_views(self._inputs)
         self.q.copy_(wl.q)
@@ -93,12 +93,20 @@ class DeviceStep:
         return out, lse
 
     def host_buffers(self):
-        """Pinned host buffers laid out like this step's device input and output groups:
-        (h_q, h_req_pool_indices, h_seq_lens, h_out, h_lse) for ``prepare_host_step``,
-        which then needs one copy in and one copy out per step."""
+        """Pinned host buffers with the packed layout of pa_decode_step_host_packed:
+        (h_inputs, h_outputs, views) with views = (h_q, h_req_pool_indices, h_seq_lens,
+        h_out, h_lse) into them."""
         h_in = torch.empty(self._input_bytes(), dtype=torch.uint8, pin_memory=True)
         h_outs = torch.empty(self._output_bytes(), dtype=torch.uint8, pin_memory=True)
-        return (*self._input_views(h_in), *self._output_views(h_outs))
+        return h_in, h_outs, (*self._input_views(h_in), *self._output_views(h_outs))
+
+    def prepare_packed_host_step(self, h_inputs, h_outputs, use_pdl=True, stream=None):
+        """A prepared ``pa_decode_step_host_packed`` call: h_inputs copied into this
+        step's input group, the step, the output group copied to h_outputs."""
+        return B.prepare_decode_step_host_packed(
+            h_inputs=h_inputs, inputs=self._inputs, h_outputs=h_outputs,
+            outputs=self._outputs, stream=B._stream(stream), use_pdl=use_pdl,
+            **self._step_kwargs())
 
     # ---- the three stages ---------------------------------------------------------
     def metadata(self, use_pdl=True, stream=None):

@@ -108,6 +108,40 @@ def test_host_step_validation(lib):
     assert lib.pa_decode_step_host(None, None, None, None, None, *empty) == B.PA_OK
 
 
+def test_packed_host_step_validation(lib):
+    # pa_decode_step's arguments without the q / index / output pointers
+    rest = [FAKE, 4, 1024, None, 0, 0, 16, FAKE, FAKE, FAKE, 16, None, 16, FAKE, FAKE, None,
+            None, 0, 2, 32, 8, 128, 64, 100, 4, 0.1, FAKE, 1 << 20, None, 1]
+    step = lambda hi=FAKE, di=FAKE, ho=FAKE, do=FAKE, bs=2: lib.pa_decode_step_host_packed(
+        hi, di, ho, do, *rest[:18], bs, *rest[19:])
+    assert step(hi=None) == B.PA_ERR_INVALID
+    assert step(do=None) == B.PA_ERR_INVALID
+    assert step(di=FAKE + 8) == B.PA_ERR_INVALID              # device buffers 16-byte aligned
+    assert step(bs=0, hi=None, di=None, ho=None, do=None) == B.PA_OK
+    # q bf16 then two int64 index vectors; out bf16 then lse fp32
+    assert lib.pa_packed_input_bytes(3, 32, 128) == 3 * 32 * 128 * 2 + 2 * 8 * 3
+    assert lib.pa_packed_output_bytes(3, 32, 128) == 3 * 32 * 128 * 2 + 4 * 3 * 32
+    assert lib.pa_packed_input_bytes(0, 32, 128) == 0
+
+
+def test_step_rejects_producer_limits_before_any_launch(lib):
+    """A decode step the selected producer cannot run is rejected on the host before the
+    metadata kernel is enqueued (here, with no GPU, an enqueue would fail as a CUDA
+    error instead)."""
+    step = lambda hq: lib.pa_decode_step(
+        FAKE, FAKE, FAKE, 4, 1024, None, 0, 0, 16, FAKE, FAKE, FAKE, 16, None, 16, FAKE, FAKE,
+        FAKE, None, None, 0, 2, hq, 2, 128, 64, 100, 4, 0.1, FAKE, 1 << 20, FAKE, None, None, 1)
+    with B.producer(B.PA_PRODUCER_FMA):
+        assert step(32) == B.PA_ERR_UNSUPPORTED                # CUDA-core producer: G <= 8
+    window = lambda **o: lib.pa_decode_step_window(
+        FAKE, FAKE, FAKE, 4, 1 << 31, FAKE, 100, 0, o.get("msp", 16), FAKE, FAKE, FAKE,
+        o.get("msp", 16), FAKE, o.get("msp", 16), FAKE, FAKE, FAKE, None, None, 0, 2, 32, 8,
+        128, 64, 100, 100, 4, 0.1, FAKE, 1 << 20, FAKE, None, None, 1)
+    assert window(msp=(1 << 23) + 1) == B.PA_ERR_UNSUPPORTED   # window bounds past 2^29
+    with B.producer(B.PA_PRODUCER_FMA):
+        assert window() == B.PA_ERR_UNSUPPORTED                # tensor-core producer only
+
+
 def test_multi_step_validation(lib):
     def step(cq=FAKE, mql=2, hq=32, bs=2, total_q=4):
         return lib.pa_decode_step_multi(

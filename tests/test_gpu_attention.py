@@ -262,25 +262,26 @@ def test_benchmark_launch_configuration_matches_oracle(name):
 
 @pytest.mark.parametrize("packed", [False, True])
 def test_host_buffer_step_matches_device_step(packed):
-    """pa_decode_step_host: host inputs copied in, the step, outputs copied back; the
-    outputs equal pa_decode_step's bit for bit, on two calls in a row with new inputs.
-    packed: host and device buffers back to back (one copy each way); else separate
-    buffers (one copy per buffer)."""
+    """pa_decode_step_host (separate buffers, one copy per buffer) and
+    pa_decode_step_host_packed (one input and one output buffer, one copy each way):
+    host inputs copied in, the step, outputs copied back; the outputs equal
+    pa_decode_step's bit for bit, on two calls in a row with new inputs."""
     wl, ds = named("bs8_ctx1k")
     for call in range(2):
         q = synthetic.draw_queries(wl.spec.bs, wl.spec.num_q_heads, wl.spec.head_dim, 70 + call)
+        ds.out.zero_()
         if packed:
-            h_q, h_rpi, h_sl, h_out, h_lse = ds.host_buffers()
+            h_in, h_outs, (h_q, h_rpi, h_sl, h_out, h_lse) = ds.host_buffers()
             h_q.copy_(q)
             h_rpi.copy_(wl.req_pool_indices)
             h_sl.copy_(wl.seq_lens)
+            ds.prepare_packed_host_step(h_in, h_outs)()
         else:
             h_q, h_rpi = q.pin_memory(), wl.req_pool_indices.clone().pin_memory()
             h_sl = wl.seq_lens.clone().pin_memory()
             h_out = torch.empty(ds.out.shape, dtype=torch.bfloat16).pin_memory()
             h_lse = torch.empty(ds.lse.shape, dtype=torch.float32).pin_memory()
-        ds.out.zero_()
-        ds.prepare_host_step(h_q, h_rpi, h_sl, h_out, h_lse)()
+            ds.prepare_host_step(h_q, h_rpi, h_sl, h_out, h_lse)()
         torch.cuda.synchronize()
         assert torch.equal(ds.q.cpu(), q)
         ds.step()
