@@ -30,15 +30,19 @@
 //     from the S^T fragments with movmatrix.trans.  Q^T fragments stay in registers for
 //     the whole split.
 //   * bf16 KV: K fragments come from ldmatrix, V^T fragments from ldmatrix.trans.
-//   * int8 KV: 16-byte shared loads of the codes, widened exactly to fp16 in registers
-//     (a byte placed in the mantissa of 1024) and fed to fp16 MMAs (int8 codes are
-//     exact in fp16; Q is rounded to fp16, exact for 2^-14 <= |q| <= 65504).  Both K
-//     and V codes enter biased by +1152: the resulting 1152 * sum(q) per column is
-//     subtracted from the fp32 score, and 1152 times each column's sum of fp16 weights
-//     (accumulated by an all-ones MMA) from the output once per split.  The contraction
-//     order over channels is permuted so that each lane reads 16 contiguous bytes;
-//     QK^T does not depend on that order.  The K scale multiplies the fp32 score, the
-//     V scale folds into the softmax weight.
+//   * int8 KV: codes widened exactly to fp16 in registers (a byte placed in the
+//     mantissa of 1024: one XOR per 4 bytes, one byte permute per fp16 pair) and fed to
+//     fp16 MMAs.  K: 16-byte shared loads, with the contraction order over channels
+//     permuted so that each lane reads 16 contiguous bytes (QK^T does not depend on
+//     that order).  V: ldmatrix.trans hands each lane two tokens of one channel, the
+//     pair an A register of V^T holds.  Both K and V codes enter biased by +1152: the
+//     resulting 1152 * sum(q) per column is subtracted from the fp32 score, and 1152
+//     times each column's sum of fp16 weights (accumulated by an all-ones MMA) from the
+//     output every kBiasPeriod chunks.  Q is scaled per column by a power of two into
+//     fp16's range (bf16 values stay exact; the factor returns in the fp32 score
+//     scale).  The K scale multiplies the fp32 score; the V scale folds into the fp16
+//     softmax weight, prescaled per warp by a power of two so that no significant
+//     weight is an fp16 subnormal.
 //   * Sliding window (kWindow): the splits cover each request's window, positions below
 //     a column's window start are masked, and pages with a -1 table entry are neither
 //     loaded nor attended.
@@ -74,9 +78,14 @@ constexpr float kMaxSlack = PA_MAX_SLACK;
 #define PA_MASK_FAST 1
 #endif
 // int8 V enters the PV product still biased by +1152 (no per-element subtract); the
-// bias is removed once per split from the column sums of the fp16 weights.
-#ifndef PA_INT8_V_BIAS
-#define PA_INT8_V_BIAS 1
+// bias is removed from the output every kBiasPeriod chunks (and at the end) using the
+// column sums of the fp16 weights, which keeps the fp32 rounding of the biased sums
+// small next to the output.
+constexpr int kBiasPeriod = 16;
+// 1: subtract the bias from the fp16 codes before the PV product instead (exact codes,
+// one fp16x2 subtract per register, no column-sum MMA).
+#ifndef PA_INT8_V_EXACT
+#define PA_INT8_V_EXACT 1
 #endif
 
 template <bool kQuant, int STAGES>
@@ -163,15 +172,11 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Two biased int8 codes (already XORed with 0x80) -> fp16x2 holding the signed codes:
-// each byte becomes the low mantissa byte of 1024, then 1152 is subtracted (exact).
-// kKeepBias: leave the +1152 in (code + 1152, also exact).
-template <bool kKeepBias>
+// Two int8 codes (already XORed with 0x80, i.e. code + 128 as unsigned bytes) picked by
+// `selector` -> fp16x2 holding code + 1152 each: the byte becomes the low mantissa byte
+// of 1024 (0x64xx), exact.
 __device__ __forceinline__ uint32_t biased_bytes_to_f16x2(uint32_t x, uint32_t selector) {
-  const uint32_t h = __byte_perm(x, 0x64646464u, selector);
-  if constexpr (kKeepBias) return h;
-  __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), __float2half2_rn(1152.f));
-  return *reinterpret_cast<uint32_t*>(&v);
+  return __byte_perm(x, 0x64646464u, selector);
 }
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-row tile written by
@@ -180,56 +185,86 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Power of two 2^e with e clamped to [-100, 100] (exact; built from the exponent bits).
+__device__ __forceinline__ float pow2_clamped(int e) {
+  e = max(-100, min(100, e));
+  return __int_as_float((e + 127) << 23);
+}
+
+// Exponent E of a finite x > 0 (x = m * 2^E, 1 <= m < 2); subnormals read as -127.
+__device__ __forceinline__ int float_exponent(float x) {
+  return ((__float_as_int(x) >> 23) & 0xff) - 127;
+}
+
 // B operand of S^T = K Q^T.  Column n of the N dimension is query i = n / G of the
 // request (row q_begin + i) and query head kvh * G + n % G; columns n >= q_len * G are
 // zero.  b0 = Q[col][k 2tig, 2tig+1], b1 = Q[col][k 2tig+8, +9] of k-step j, for
-// column n = 8 * nt + gid.  int8 path (kF16): fp16 Q in the permuted contraction order
-// (k-step j, lane tig -> channels 32*tig + 4*j + {0..3}), plus kbias: the K codes enter
-// the MMA biased by +1152 (the widening skips the subtract), so each score carries
-// 1152 * sum_d q[col][d]; kbias[nt][e] (column 8nt + 2tig + e) is that offset from the
-// same fp16 Q values.  The whole warp calls this.
+// column n = 8 * nt + gid.  qf[nt][e]: the fp32 factor that turns column 8nt + 2tig + e
+// of the MMA result into a base-2 score (q_scale, times the column's Q prescale below).
+// int8 path (kF16): fp16 Q in the permuted contraction order (k-step j, lane tig ->
+// channels 32*tig + 4*j + {0..3}).  Each column is first scaled by a power of two that
+// puts its largest |q| in [2^14, 2^15) (exact for bf16 values, and no |q| can overflow
+// fp16's 65504); qf undoes it.  kbias: the K codes enter the MMA biased by +1152 (the
+// widening skips the subtract), so each score carries 1152 * sum_d q[col][d];
+// kbias[nt][e] is that offset from the same fp16 Q values.  The whole warp calls this.
 template <bool kF16, int kNT>
 __device__ __forceinline__ void load_q_fragments(const SplitKParams& prm, int q_begin, int q_len,
                                                  int kvh, int G, int gid, int tig,
                                                  uint32_t (&qb)[kNT][8][2],
-                                                 float (&kbias)[kNT][2]) {
+                                                 float (&kbias)[kNT][2], float (&qf)[kNT][2]) {
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) {
     const int col = 8 * nt + gid;
     const int qi = col / G;
     const int head = kvh * G + (col - qi * G);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t lo = 0, hi = 0;
-      if (col < q_len * G) {
-        const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(prm.q) +
-                                  (static_cast<int64_t>(q_begin + qi) * prm.num_q_heads + head) * 128;
-        if constexpr (kF16) {
-          const int d = 32 * tig + 4 * j;
-          lo = pack_f16(__bfloat162float(qr[d]), __bfloat162float(qr[d + 1]));
-          hi = pack_f16(__bfloat162float(qr[d + 2]), __bfloat162float(qr[d + 3]));
-        } else {
-          const int d = 16 * j + 2 * tig;
-          lo = *reinterpret_cast<const uint32_t*>(qr + d);
-          hi = *reinterpret_cast<const uint32_t*>(qr + d + 8);
-        }
-      }
-      qb[nt][j][0] = lo;
-      qb[nt][j][1] = hi;
-    }
-    kbias[nt][0] = kbias[nt][1] = 0.f;
+    const bool live = col < q_len * G;
+    const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(prm.q) +
+                              (static_cast<int64_t>(q_begin + qi) * prm.num_q_heads + head) * 128;
     if constexpr (kF16) {
+      float v[8][4];
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          v[j][u] = live ? __bfloat162float(qr[32 * tig + 4 * j + u]) : 0.f;
+          amax = fmaxf(amax, fabsf(v[j][u]));
+        }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));  // over the 128 channels
+      const int e = amax > 0.f ? 14 - float_exponent(amax) : 0;
+      const float up = pow2_clamped(e);
       float part = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
+        qb[nt][j][0] = pack_f16(v[j][0] * up, v[j][1] * up);
+        qb[nt][j][1] = pack_f16(v[j][2] * up, v[j][3] * up);
         const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qb[nt][j][0]));
         const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&qb[nt][j][1]));
         part += (a.x + a.y) + (c.x + c.y);
       }
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);  // sum over the column's 128 channels
-      kbias[nt][0] = 1152.f * __shfl_sync(0xffffffffu, part, (2 * tig) * 4);
-      kbias[nt][1] = 1152.f * __shfl_sync(0xffffffffu, part, (2 * tig + 1) * 4);
+      const float down = prm.q_scale * pow2_clamped(-e);
+#pragma unroll
+      for (int ee = 0; ee < 2; ++ee) {
+        kbias[nt][ee] = 1152.f * __shfl_sync(0xffffffffu, part, (2 * tig + ee) * 4);
+        qf[nt][ee] = __shfl_sync(0xffffffffu, down, (2 * tig + ee) * 4);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t lo = 0, hi = 0;
+        if (live) {
+          const int d = 16 * j + 2 * tig;
+          lo = *reinterpret_cast<const uint32_t*>(qr + d);
+          hi = *reinterpret_cast<const uint32_t*>(qr + d + 8);
+        }
+        qb[nt][j][0] = lo;
+        qb[nt][j][1] = hi;
+      }
+      kbias[nt][0] = kbias[nt][1] = 0.f;
+      qf[nt][0] = qf[nt][1] = prm.q_scale;
     }
   }
 }
@@ -283,14 +318,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
   };
 
-  // ---- prologue independent of the metadata stage: Q^T fragments in registers ------
-  // (with several queries per request their rows come from cu_seqlens_q, a metadata
-  // output, so Q is loaded after the wait instead)
-  const int b = blockIdx.z;
-  const bool multi = prm.cu_seqlens_q != nullptr;
-  uint32_t qb[kNT][8][2];
-  float kbias[kNT][2];
-  if (!multi && is_consumer) load_q_fragments<kF16, kNT>(prm, b, 1, kvh, G, gid, tig, qb, kbias);
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -301,10 +328,25 @@ __global__ void __launch_bounds__(kThreads, MINB)
     *producer_done = 0;
     fence_barrier_init();
   }
+  __syncthreads();  // barriers initialised; no global load has been issued yet
+
+  // ---- consumers: Q^T fragments in registers, independent of the metadata stage -----
+  // (with several queries per request their rows come from cu_seqlens_q, a metadata
+  // output, so Q is loaded after the wait instead).  The TMA warp does not wait for
+  // this: it goes straight to the split's length and page indices and starts copying.
+  const int b = blockIdx.z;
+  const bool multi = prm.cu_seqlens_q != nullptr;
+  uint32_t qb[kNT][8][2];
+  float kbias[kNT][2], qf[kNT][2];
+  if (!multi && is_consumer)
+    load_q_fragments<kF16, kNT>(prm, b, 1, kvh, G, gid, tig, qb, kbias, qf);
 
   // ---- everything below reads what the metadata stage wrote -------------------------
   grid_dependency_wait();
-  PA_TS_FIRST(prm.ts, 1, kTsReady);
+#ifdef PA_TIMESTAMPS
+  if (prm.ts != nullptr && tid == kConsumerWarps * 32)
+    atomicMin(prm.ts + 3 * 1 + kTsReady, global_timer_ns());
+#endif
 
   int q_begin = b, q_len = 1;
   if (multi) {
@@ -314,14 +356,16 @@ __global__ void __launch_bounds__(kThreads, MINB)
       if (tid == 0 && split == 0 && kvh == 0) record_error(prm.err, kErrSeqLenOutOfRange);
       q_len = q_len < 0 ? 0 : prm.max_q_len;
     }
-    if (is_consumer) load_q_fragments<kF16, kNT>(prm, q_begin, q_len, kvh, G, gid, tig, qb, kbias);
+    if (is_consumer)
+      load_q_fragments<kF16, kNT>(prm, q_begin, q_len, kvh, G, gid, tig, qb, kbias, qf);
   }
   const int ncols = q_len * G;  // (query, head) columns of this request and kv head
 
   // Without a window the split's page indices and the request length are independent
-  // loads: issue both before either is used (page indices are bounds-checked where they
-  // are used).  With a window the split starts at the page of the request's first
-  // visible position, which depends on the length.
+  // loads: the TMA warp issues both before either is used (page indices are
+  // bounds-checked where they are used).  With a window the split starts at the page of
+  // the request's first visible position, which depends on the length.  Only the TMA
+  // warp reads the page indices.
   const int window = kWindow ? prm.window : 0;
   int p_begin = split * prm.pages_per_split;
   const int32_t* pt_row = prm.page_table + static_cast<int64_t>(b) * prm.page_table_stride;
@@ -329,9 +373,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
     pt_row += p_begin;
     const int pages_cap =
         min(min(prm.pages_per_split, prm.max_seq_pages - p_begin), kMaxSplitPages);
-    for (int i = tid; i < pages_cap; i += kThreads) pages_s[i] = pt_row[i];
+    for (int i = lane; i < pages_cap; i += 32) pages_s[i] = pt_row[i];
   };
-  if (window == 0) cache_page_indices();
+  if (window == 0 && !is_consumer) cache_page_indices();
   int n = prm.cache_seqlens[b];
   const int cap = prm.max_seq_pages * P;
   if (n < 0 || n > cap) {
@@ -340,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   }
   if (window > 0) {
     p_begin += max(0, n - q_len - window + 1) / P;
-    cache_page_indices();
+    if (!is_consumer) cache_page_indices();
   }
   const int n_pages = (n + P - 1) / P;
   const int p_end = min(p_begin + prm.pages_per_split, n_pages);
@@ -359,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   }
 
   const int n_split_pages = p_end - p_begin;
-  __syncthreads();  // barriers initialised, page indices cached
+  if (!is_consumer) __syncwarp();  // the TMA warp's page indices, cached by its lanes
 
   const int n_chunks = (n_tok + kChunk - 1) / kChunk;
 
@@ -492,12 +536,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
   for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
-  // int8 with the V bias kept: per column, the sum of the fp16 weights that entered the
-  // PV product (every row of the fragment holds the same sums); O = O_biased - 1152 sum.
-  constexpr bool kVBias = kQuant && PA_INT8_V_BIAS;
+  // int8: per column, the sum of the fp16 weights that entered the PV product since the
+  // last bias removal (every row of the fragment holds the same sums); O = O_biased -
+  // 1152 sum.
+  constexpr bool kVBias = kQuant && !PA_INT8_V_EXACT;
   float wsum[kNT][4];
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) wsum[nt][0] = wsum[nt][1] = wsum[nt][2] = wsum[nt][3] = 0.f;
+  // int8: the fp16 PV weights are p * v_scale * vmul, with vmul a warp-uniform power of
+  // two that puts the largest V scale seen so far in [64, 128): weights stay below
+  // 2^kMaxSlack * 128 (no fp16 overflow) and every weight within 2^-20 of the largest
+  // one is a normal fp16 number (no subnormal rounding).  o and wsum are in those units;
+  // vmul only shrinks (exact rescale) when a larger scale appears.  0: not set yet.
+  float vmul = 0.f;
   // softmax state of heads 8*nt + 2*tig + e (identical in the 8 lanes sharing tig)
   // m_run: the reference maximum the weights are relative to (warp-uniform per column);
   // t_max: this thread's true maximum of its own scores, reduced once per split.
@@ -508,7 +559,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
     t_max[nt][0] = t_max[nt][1] = -CUDART_INF_F;
     l_part[nt][0] = l_part[nt][1] = 0.f;
   }
-  const float q_scale = prm.q_scale;
   const int t0 = warp * 16;  // this warp's tokens inside every chunk
   bool failed = false;
   // Causal limit of this thread's columns, in token positions of the split: query i of a
@@ -550,8 +600,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
     if (active) {
       // Rows of this warp's slice past the context: their V bytes are not ours to trust
-      // (stale ring contents or cache slots past the request), so zero them before PV.
-      if (partial) {
+      // (stale ring contents or cache slots past the request), so zero them before PV
+      // (bf16: 0 * NaN would poison the output).  int8 needs none of it: every byte
+      // widens to a finite fp16 number and those rows have weight 0.
+      if (!kQuant && partial) {
         for (int r = max(valid, t0) + (lane >> 3); r < t0 + 16; r += 4) {
           uint4* row = reinterpret_cast<uint4*>(st + L::KV_BYTES + r * 128);
           row[lane & 7] = make_uint4(0u, 0u, 0u, 0u);
@@ -614,6 +666,30 @@ __global__ void __launch_bounds__(kThreads, MINB)
         ks_b = kscale[tok_b];
         vs_a = tok_a < valid ? vscale[tok_a] : 0.f;
         vs_b = tok_b < valid ? vscale[tok_b] : 0.f;
+        const float vhi = fmaxf(vs_a, vs_b);
+        if (__any_sync(0xffffffffu, vmul == 0.f || vhi * vmul >= 128.f)) {
+          float vmax = vhi;  // over the warp's 16 tokens
+#pragma unroll
+          for (int m = 4; m <= 16; m <<= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, m));
+          if (vmax > 0.f) {
+            const float vmul_new = pow2_clamped(6 - float_exponent(vmax));
+            if (vmul != 0.f && vmul_new < vmul) {
+              const float r = vmul_new / vmul;  // a power of two: exact
+#pragma unroll
+              for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                  for (int r4 = 0; r4 < 4; ++r4) o[nt][i][r4] *= r;
+#pragma unroll
+                for (int r4 = 0; r4 < 4; ++r4) wsum[nt][r4] *= r;
+              }
+            }
+            if (vmul == 0.f || vmul_new < vmul) vmul = vmul_new;
+          }
+        }
+        vs_a *= vmul;
+        vs_b *= vmul;
       }
       uint32_t pb[kNT][2];
       // every score of a full slice of a one-query split without a window is visible
@@ -626,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int i = 0; i < 4; ++i) {
           float v = (acc[0][nt][i] + acc[1][nt][i]);
           if constexpr (kQuant) v -= kbias[nt][i & 1];
-          v *= q_scale;
+          v *= qf[nt][i & 1];
           if constexpr (kQuant) v *= (i < 2 ? ks_a : ks_b);
           x[i] = v;
         }
@@ -701,33 +777,31 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
       // ---- O^T += V^T P^T (M = 16 channels per tile, K = 16 tokens) ----------------------
       if constexpr (kQuant) {
-        // V rows t0 + 2tig + {0, 1, 8, 9}, channels 16*gid .. 16*gid + 15; M-tile i row
-        // gid is channel 16*gid + 2i, row gid + 8 is channel 16*gid + 2i + 1.
-        const int r0 = t0 + 2 * tig;
-        const uint4 va = *reinterpret_cast<const uint4*>(st + L::KV_BYTES + swz(r0, gid));
-        const uint4 vb = *reinterpret_cast<const uint4*>(st + L::KV_BYTES + swz(r0 + 1, gid));
-        const uint4 vc = *reinterpret_cast<const uint4*>(st + L::KV_BYTES + swz(r0 + 8, gid));
-        const uint4 vd = *reinterpret_cast<const uint4*>(st + L::KV_BYTES + swz(r0 + 9, gid));
-        const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
-        const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+        // ldmatrix.trans of (8 tokens x 16 bytes) matrices: lane (gid, tig) receives the
+        // bytes of channels 16i + 2gid, +1 for tokens 2tig, 2tig + 1 of the matrix, so one
+        // byte permute per fp16x2 gives an A register of V^T (two tokens of one channel).
+        // M-tile i row gid is channel 16i + 2gid, row gid + 8 is channel 16i + 2gid + 1.
+        // Matrices per x4 load: tokens t0..+7 / t0+8..+15 of chunk 2ii, then of 2ii + 1.
+        const int mrow = t0 + (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t xa = wa[w] ^ 0x80808080u, xb = wb[w] ^ 0x80808080u;
-          const uint32_t xc = wc[w] ^ 0x80808080u, xd = wd[w] ^ 0x80808080u;
-          const uint32_t ab_lo = __byte_perm(xa, xb, 0x5140), ab_hi = __byte_perm(xa, xb, 0x7362);
-          const uint32_t cd_lo = __byte_perm(xc, xd, 0x5140), cd_hi = __byte_perm(xc, xd, 0x7362);
-          uint32_t a_even[4] = {biased_bytes_to_f16x2<kVBias>(ab_lo, 0x4140),
-                                biased_bytes_to_f16x2<kVBias>(ab_lo, 0x4342),
-                                biased_bytes_to_f16x2<kVBias>(cd_lo, 0x4140),
-                                biased_bytes_to_f16x2<kVBias>(cd_lo, 0x4342)};
-          uint32_t a_odd[4] = {biased_bytes_to_f16x2<kVBias>(ab_hi, 0x4140),
-                               biased_bytes_to_f16x2<kVBias>(ab_hi, 0x4342),
-                               biased_bytes_to_f16x2<kVBias>(cd_hi, 0x4140),
-                               biased_bytes_to_f16x2<kVBias>(cd_hi, 0x4342)};
+        for (int ii = 0; ii < 4; ++ii) {
+          uint32_t x[4];
+          ldsm_x4_trans(vst + swz(mrow, 2 * ii + (lane >> 4)), x[0], x[1], x[2], x[3]);
 #pragma unroll
-          for (int nt = 0; nt < kNT; ++nt) {
-            mma16816<true>(o[nt][2 * w], a_even, pb[nt][0], pb[nt][1]);
-            mma16816<true>(o[nt][2 * w + 1], a_odd, pb[nt][0], pb[nt][1]);
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t xa = x[2 * h] ^ 0x80808080u, xb = x[2 * h + 1] ^ 0x80808080u;
+            uint32_t a[4] = {biased_bytes_to_f16x2(xa, 0x4240), biased_bytes_to_f16x2(xa, 0x4341),
+                             biased_bytes_to_f16x2(xb, 0x4240), biased_bytes_to_f16x2(xb, 0x4341)};
+            if constexpr (!kVBias) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&a[u]),
+                                          __floats2half2_rn(1152.f, 1152.f));
+                a[u] = *reinterpret_cast<const uint32_t*>(&v);
+              }
+            }
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) mma16816<true>(o[nt][2 * ii + h], a, pb[nt][0], pb[nt][1]);
           }
         }
         if constexpr (kVBias) {
@@ -752,9 +826,22 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
     // this warp is done with the stage; zeroing stores (generic proxy) must be ordered
     // before the TMA (async proxy) refills the buffer
-    if (active && partial) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (!kQuant && active && partial) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
+    if constexpr (kVBias) {
+      if (c % kBiasPeriod == kBiasPeriod - 1) {
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int r4 = 0; r4 < 4; ++r4) o[nt][i][r4] -= 1152.f * wsum[nt][r4];
+#pragma unroll
+          for (int r4 = 0; r4 < 4; ++r4) wsum[nt][r4] = 0.f;
+        }
+      }
+    }
   }
 
   trigger_dependents();
@@ -813,12 +900,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
         float mrow = -CUDART_INF_F;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + head) * 3 + 2]);
-        const float scale = m_run[nt][e] == -CUDART_INF_F ? 0.f : exp2f(m_run[nt][e] - mrow);
+        float scale = m_run[nt][e] == -CUDART_INF_F ? 0.f : exp2f(m_run[nt][e] - mrow);
+        if constexpr (kQuant) scale = vmul > 0.f ? scale / vmul : 0.f;  // vmul: power of two
         float* dst = red + (warp * 16 + head) * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int ch0 = kQuant ? 16 * gid + 2 * i : 16 * i + gid;
-          const int ch1 = kQuant ? 16 * gid + 2 * i + 1 : 16 * i + gid + 8;
+          const int ch0 = kQuant ? 16 * i + 2 * gid : 16 * i + gid;
+          const int ch1 = kQuant ? 16 * i + 2 * gid + 1 : 16 * i + gid + 8;
           float v0 = o[nt][i][e], v1 = o[nt][i][2 + e];
           if constexpr (kVBias) {
             v0 -= 1152.f * wsum[nt][e];

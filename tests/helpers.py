@@ -16,8 +16,15 @@ Attention tolerance against the float64 oracle (``out_tolerance``):
   the V scale to fp16, u_w = 2^-11), so the output is ``sum_j p_j (1 + d_j) v_j / l``
   with |d_j| <= u_w, off by at most ``u_w * A``.  The 2^-13 * A term covers the fp32
   parts (score rounding, exp2, accumulation and the split merges, each a relative
-  error far below 2^-13 at these sizes).  ``ulp(|ref| + E)`` allows for the computed
-  value lying across a binade boundary from the reference.
+  error far below 2^-13 at these sizes; the int8 producer removes its +1152 V bias
+  every 16 chunks so its biased sums stay within that).  ``ulp(|ref| + E)`` allows for
+  the computed value lying across a binade boundary from the reference.
+  int8 adds one absolute term: the fp16 weights are scaled so that the largest V scale
+  seen maps to [64, 128), and a weight below fp16's normal range (2^-14, i.e. more
+  than 2^-20 below the largest) is rounded with absolute error <= 2^-25 in those units,
+  2^-31 * max(v_scale) in V units per unit code; over n <= max(cache_seqlens) tokens of
+  codes <= 127 and a normaliser >= 1 that is at most ``2^-31 * max(v_scale) * 127 * n``
+  (``Expected.abs_floor``).
 """
 
 from __future__ import annotations
@@ -53,7 +60,8 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, e - 8)
 
 
-def out_tolerance(ref: np.ndarray, abs_ref: np.ndarray | None, weight: str) -> np.ndarray:
+def out_tolerance(ref: np.ndarray, abs_ref: np.ndarray | None, weight: str,
+                  abs_floor: float = 0.0) -> np.ndarray:
     """Per-element O bound (see the module docstring); ``abs_ref`` is needed only where
     |ref| >= 4."""
     tol = np.full(ref.shape, O_ATOL)
@@ -61,9 +69,17 @@ def out_tolerance(ref: np.ndarray, abs_ref: np.ndarray | None, weight: str) -> n
     if big.any():
         if abs_ref is None:
             raise AssertionError("reference values >= 4 need the oracle's |V| output")
-        e = (WEIGHT_UNIT[weight] + FP32_MARGIN) * abs_ref[big]
+        e = (WEIGHT_UNIT[weight] + FP32_MARGIN) * abs_ref[big] + abs_floor
         tol[big] = 0.5 * bf16_ulp(np.abs(ref[big]) + e) + e
     return tol
+
+
+def subnormal_floor(weight: str, v_scale, cache_seqlens) -> float:
+    """The int8 producer's absolute bound for PV weights below fp16's normal range (see
+    the module docstring); 0 for other weight types."""
+    if weight != "int8" or v_scale is None or np.size(cache_seqlens) == 0:
+        return 0.0
+    return 2.0 ** -31 * float(np.max(v_scale)) * 127.0 * float(max(1, np.max(cache_seqlens)))
 
 
 def abs_values(v: np.ndarray) -> np.ndarray:
@@ -86,6 +102,10 @@ class Expected:
         self.weight = weight or ("int8" if v.dtype == np.int8 else "bf16")
         self.out, self.lse = fn(*args, **kwargs)
         self._abs = None
+        # v_scale is the last positional argument and cache_seqlens the fifth of every
+        # oracle attention function
+        self.abs_floor = subnormal_floor(self.weight, args[-1], args[4]) \
+            if self.weight == "int8" else 0.0
 
     def abs_out(self) -> np.ndarray:
         if self._abs is None:
@@ -163,6 +183,38 @@ def oracle_partials(wl, meta, num_splits, rows=None, v_override=None):
                                   wl.sm_scale, wl.max_seq_pages, num_splits, ks, vs)
 
 
+def assert_partials_close(m, l, acc, m_ref, l_ref, acc_ref, acc_abs, weight, what="",
+                          abs_floor=0.0):
+    """Split partials (m natural-log max, l sum of exponentials, acc unnormalised output)
+    against the oracle's: m within 1e-4 (relative, at least 1e-4 absolute), l within 1e-4
+    relative, and acc = sum_j p_j v_j within (u_w + 2^-13) * sum_j p_j |v_j| (each PV
+    weight rounded once to the MMA operand type, the rest fp32; ``acc_abs`` is the
+    oracle's acc over |V|, same split partition and maximum; ``abs_floor``: the int8
+    subnormal-weight term, ``subnormal_floor``).  Empty splits: m = -inf, l = 0."""
+    m, l, acc = (np.asarray(t, np.float64) for t in (m, l, acc))
+    empty = np.isneginf(m_ref)
+    assert np.array_equal(np.isneginf(m), empty), f"{what}: empty-split pattern differs"
+    assert np.all(l[empty] == 0), f"{what}: empty split with l != 0"
+    full = ~empty
+    if not full.any():
+        return
+    m_err = np.abs(m[full] - m_ref[full]).max()
+    assert m_err <= 1e-4 * max(1.0, np.abs(m_ref[full]).max()), f"{what}: m err {m_err}"
+    l_rel = (np.abs(l[full] - l_ref[full]) / l_ref[full]).max()
+    assert l_rel <= 1e-4, f"{what}: l relative err {l_rel}"
+    err = np.abs(acc[full] - acc_ref[full])
+    tol = (WEIGHT_UNIT[weight] + FP32_MARGIN) * acc_abs[full] + abs_floor + 1e-30
+    ratio = err / tol
+    if ratio.max() > 1:
+        i = np.unravel_index(np.argmax(ratio), ratio.shape)
+        raise AssertionError(
+            f"{what}: acc error {err[i]:.3e} > bound {tol[i]:.3e} (ratio {ratio[i]:.2f}) at "
+            f"split row {i[0]} channel {i[1]}: got {acc[full][i]:.6e}, oracle "
+            f"{acc_ref[full][i]:.6e}, oracle over |V| {acc_abs[full][i]:.6e}, l "
+            f"{l_ref[full][i[0]]:.6e}, m {m_ref[full][i[0]]:.6f}; err/acc_abs max "
+            f"{(err / np.maximum(acc_abs[full], 1e-30)).max():.3e}")
+
+
 def band_errors(o: np.ndarray, ref: np.ndarray) -> dict:
     """Max |o - ref| per |ref| band (bands with no element are left out)."""
     err = np.abs(o - ref)
@@ -178,9 +230,10 @@ def band_errors(o: np.ndarray, ref: np.ndarray) -> dict:
 def assert_attention_close(out_gpu, lse_gpu, ref, what=""):
     """``ref``: an ``Expected`` (or an (out, lse) pair when every |ref| < 4)."""
     if isinstance(ref, tuple):
-        out_ref, lse_ref, abs_fn, weight = ref[0], ref[1], None, "bf16"
+        out_ref, lse_ref, abs_fn, weight, floor = ref[0], ref[1], None, "bf16", 0.0
     else:
         out_ref, lse_ref, abs_fn, weight = ref.out, ref.lse, ref.abs_out, ref.weight
+        floor = ref.abs_floor
     o = out_gpu.float().cpu().numpy().astype(np.float64)
     lse = lse_gpu.float().cpu().numpy().astype(np.float64)
     empty = np.isneginf(lse_ref)
@@ -193,7 +246,7 @@ def assert_attention_close(out_gpu, lse_gpu, ref, what=""):
     o_f, r_f = o[full], out_ref[full]
     big = np.abs(r_f) >= ULP_BAND
     abs_f = abs_fn()[full] if big.any() else None
-    tol = out_tolerance(r_f, abs_f, weight)
+    tol = out_tolerance(r_f, abs_f, weight, floor)
     err = np.abs(o_f - r_f)
     o_err = float(err.max())
     l_err = float(np.abs(lse[full] - lse_ref[full]).max())

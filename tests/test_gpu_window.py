@@ -12,8 +12,8 @@ from paged_kv_decode_metadata_gb300 import binding as B
 from paged_kv_decode_metadata_gb300 import build, synthetic
 from paged_kv_decode_metadata_gb300.runtime import WindowStep
 
-from helpers import (FP32_MARGIN, WEIGHT_UNIT, Expected, abs_values, assert_attention_close,
-                     bits, oracle_metadata, paged_attention_window_threaded)
+from helpers import (Expected, abs_values, assert_attention_close, assert_partials_close, bits,
+                     oracle_metadata, paged_attention_window_threaded, subnormal_floor)
 
 pytestmark = pytest.mark.gpu
 
@@ -114,21 +114,11 @@ def test_window_partials_match_oracle(seed, kv, grp, P, window, mql, holes, spli
     m_ref, l_ref, acc_ref = oracle.splitk_partials_window(
         bits(q), k, v, table, meta["cache_seqlens"], window, wl.sm_scale, wl.max_seq_pages,
         splits, cu_q, mql or 1, ks, vs)
-    m, l, acc = (t.double().cpu().numpy() for t in (m, l, acc))
-    empty = np.isneginf(m_ref)
-    assert np.array_equal(np.isneginf(m), empty)
-    assert np.all(l[empty] == 0)
-    full = ~empty
-    assert np.abs(m[full] - m_ref[full]).max() <= 1e-4 * max(1.0, np.abs(m_ref[full]).max())
-    assert np.all(np.abs(l[full] - l_ref[full]) <= 1e-4 * l_ref[full])
-    # acc = sum_j p_j v_j, each weight rounded once to the MMA operand type (unit
-    # roundoff u_w: bf16 2^-8, fp16 2^-11) and summed in fp32: |error| <=
-    # (u_w + 2^-13) * sum_j p_j |v_j|, that sum from the oracle's partials over |V|
     _, _, acc_abs = oracle.splitk_partials_window(
         bits(q), k, abs_values(v), table, meta["cache_seqlens"], window, wl.sm_scale,
         wl.max_seq_pages, splits, cu_q, mql or 1, ks, vs)
-    tol = (WEIGHT_UNIT[kv] + FP32_MARGIN) * acc_abs[full] + 1e-30
-    assert np.all(np.abs(acc[full] - acc_ref[full]) <= tol)
+    assert_partials_close(m.cpu(), l.cpu(), acc.cpu(), m_ref, l_ref, acc_ref, acc_abs, kv,
+                          wl.spec.name, subnormal_floor(kv, vs, meta["cache_seqlens"]))
 
 
 def test_every_page_skipped_gives_empty_rows():
