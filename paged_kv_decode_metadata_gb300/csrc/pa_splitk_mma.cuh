@@ -87,6 +87,12 @@ constexpr int kBiasPeriod = 16;
 #ifndef PA_INT8_V_EXACT
 #define PA_INT8_V_EXACT 1
 #endif
+// 1: the PV weights enter as two MMA operands, the weight rounded to the operand type
+// and its rounding residual rounded again (bf16: ~2^-16 relative, fp16: ~2^-22), which
+// keeps the output error well inside the output's own rounding; 0: one operand.
+#ifndef PA_P_SPLIT
+#define PA_P_SPLIT 1
+#endif
 
 template <bool kQuant, int STAGES>
 struct Layout {
@@ -691,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         vs_a *= vmul;
         vs_b *= vmul;
       }
-      uint32_t pb[kNT][2];
+      uint32_t pb[kNT][2], pl[kNT][2];  // weights (B operand) and their residuals
       // every score of a full slice of a one-query split without a window is visible
       // (columns past the request's heads carry zero queries and are never written)
       const bool need_mask = !PA_MASK_FAST || partial || multi || check_lo;
@@ -764,15 +770,31 @@ __global__ void __launch_bounds__(kThreads, MINB)
         // P^T as the B operand of O^T += V^T P^T: transpose the two 8x8 (token, head)
         // blocks in registers.
         uint32_t xa, xb;
+        uint32_t ra = 0u, rb = 0u;
         if constexpr (kQuant) {
-          xa = pack_f16(p[0] * vs_a, p[1] * vs_a);
-          xb = pack_f16(p[2] * vs_b, p[3] * vs_b);
+          const float w0 = p[0] * vs_a, w1 = p[1] * vs_a, w2 = p[2] * vs_b, w3 = p[3] * vs_b;
+          xa = pack_f16(w0, w1);
+          xb = pack_f16(w2, w3);
+          if constexpr (PA_P_SPLIT) {
+            const float2 ha = __half22float2(*reinterpret_cast<const __half2*>(&xa));
+            const float2 hb = __half22float2(*reinterpret_cast<const __half2*>(&xb));
+            ra = pack_f16(w0 - ha.x, w1 - ha.y);
+            rb = pack_f16(w2 - hb.x, w3 - hb.y);
+          }
         } else {
           xa = pack_bf16(p[0], p[1]);
           xb = pack_bf16(p[2], p[3]);
+          if constexpr (PA_P_SPLIT) {
+            ra = pack_bf16(p[0] - bf16_lo(xa), p[1] - bf16_hi(xa));
+            rb = pack_bf16(p[2] - bf16_lo(xb), p[3] - bf16_hi(xb));
+          }
         }
         pb[nt][0] = movmatrix_trans(xa);
         pb[nt][1] = movmatrix_trans(xb);
+        if constexpr (PA_P_SPLIT) {
+          pl[nt][0] = movmatrix_trans(ra);
+          pl[nt][1] = movmatrix_trans(rb);
+        }
       }
 
       // ---- O^T += V^T P^T (M = 16 channels per tile, K = 16 tokens) ----------------------
@@ -801,14 +823,20 @@ __global__ void __launch_bounds__(kThreads, MINB)
               }
             }
 #pragma unroll
-            for (int nt = 0; nt < kNT; ++nt) mma16816<true>(o[nt][2 * ii + h], a, pb[nt][0], pb[nt][1]);
+            for (int nt = 0; nt < kNT; ++nt) {
+              mma16816<true>(o[nt][2 * ii + h], a, pb[nt][0], pb[nt][1]);
+              if constexpr (PA_P_SPLIT) mma16816<true>(o[nt][2 * ii + h], a, pl[nt][0], pl[nt][1]);
+            }
           }
         }
         if constexpr (kVBias) {
           // column sums of the fp16 weights: an all-ones A operand (fp16 1.0 = 0x3C00)
           const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
 #pragma unroll
-          for (int nt = 0; nt < kNT; ++nt) mma16816<true>(wsum[nt], ones, pb[nt][0], pb[nt][1]);
+          for (int nt = 0; nt < kNT; ++nt) {
+            mma16816<true>(wsum[nt], ones, pb[nt][0], pb[nt][1]);
+            if constexpr (PA_P_SPLIT) mma16816<true>(wsum[nt], ones, pl[nt][0], pl[nt][1]);
+          }
         }
       } else {
         const int mi = lane >> 3;
@@ -820,7 +848,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
           uint32_t a[4];
           ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
 #pragma unroll
-          for (int nt = 0; nt < kNT; ++nt) mma16816<false>(o[nt][i], a, pb[nt][0], pb[nt][1]);
+          for (int nt = 0; nt < kNT; ++nt) {
+            mma16816<false>(o[nt][i], a, pb[nt][0], pb[nt][1]);
+            if constexpr (PA_P_SPLIT) mma16816<false>(o[nt][i], a, pl[nt][0], pl[nt][1]);
+          }
         }
       }
     }

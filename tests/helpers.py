@@ -11,20 +11,23 @@ Attention tolerance against the float64 oracle (``out_tolerance``):
   ``ulp_bf16(|ref| + E) / 2 + E`` with ``E = (u_w + 2^-13) * A``, where
   ``A[c] = sum_j softmax_j |v_j[c]|`` is the oracle's output with every V element
   replaced by its magnitude.  Derivation: the producer accumulates the normaliser
-  ``l`` from the fp32 weights p_j but feeds the PV product weights rounded once to the
-  MMA operand type (bf16 KV: p_j to bf16, unit roundoff u_w = 2^-8; int8 KV: p_j times
-  the V scale to fp16, u_w = 2^-11), so the output is ``sum_j p_j (1 + d_j) v_j / l``
-  with |d_j| <= u_w, off by at most ``u_w * A``.  The 2^-13 * A term covers the fp32
-  parts (score rounding, exp2, accumulation and the split merges, each a relative
-  error far below 2^-13 at these sizes; the int8 producer removes its +1152 V bias
-  every 16 chunks so its biased sums stay within that).  ``ulp(|ref| + E)`` allows for
-  the computed value lying across a binade boundary from the reference.
+  ``l`` from the fp32 weights p_j and feeds the PV product each weight as two MMA
+  operands, the weight rounded to the operand type and its rounding residual rounded
+  again (bf16 KV: p_j, relative error u_w <= 2^-8 * 2^-8 = 2^-16; int8 KV: p_j times
+  the V scale in fp16, u_w <= 2^-11 * 2^-11 = 2^-22); int8 codes are exact in fp16.
+  So the output is ``sum_j p_j (1 + d_j) v_j / l`` with |d_j| <= u_w, off by at most
+  ``u_w * A``.  The 2^-13 * A term covers the fp32 parts (score rounding, exp2, the
+  MMA accumulation over a split's 16-token slices and the split merges; each is a
+  relative error far below 2^-13 for scores of magnitude below ~100 and splits below
+  ~65536 tokens).  ``ulp(|ref| + E)`` allows for the computed value lying across a
+  binade boundary from the reference.
   int8 adds one absolute term: the fp16 weights are scaled so that the largest V scale
-  seen maps to [64, 128), and a weight below fp16's normal range (2^-14, i.e. more
-  than 2^-20 below the largest) is rounded with absolute error <= 2^-25 in those units,
-  2^-31 * max(v_scale) in V units per unit code; over n <= max(cache_seqlens) tokens of
-  codes <= 127 and a normaliser >= 1 that is at most ``2^-31 * max(v_scale) * 127 * n``
-  (``Expected.abs_floor``).
+  seen maps to [64, 128), and a weight part below fp16's normal range (2^-14) is
+  rounded with absolute error <= 2^-25 in those units, 2^-31 * max(v_scale) in V units
+  per unit code; over n <= max(cache_seqlens) tokens of codes <= 127 and a normaliser
+  >= 1 that is at most ``2^-31 * max(v_scale) * 127 * n`` (``Expected.abs_floor``).
+  Below |ref| = 4 these bounds are at most 2^-7 + 1.4e-4 * A + the floor, inside 1e-2
+  for any |V| <= 15: the literal bound is guaranteed, not just observed.
 """
 
 from __future__ import annotations
@@ -42,9 +45,10 @@ O_ATOL = 1e-2
 LSE_ATOL = 1e-3
 # |ref| from which half a bf16 ulp (2^-6 at 4) exceeds O_ATOL
 ULP_BAND = 4.0
-# unit roundoff of the PV weights in the tensor-core producer, by KV type; "fp32" for
-# arithmetic that rounds no weight (the reducer alone)
-WEIGHT_UNIT = {"bf16": 2.0 ** -8, "int8": 2.0 ** -11, "fp32": 0.0}
+# relative error of the PV weights in the tensor-core producer (a weight and its residual,
+# each rounded to the MMA operand type), by KV type; "fp32" for arithmetic that rounds
+# no weight (the reducer alone)
+WEIGHT_UNIT = {"bf16": 2.0 ** -16, "int8": 2.0 ** -22, "fp32": 0.0}
 FP32_MARGIN = 2.0 ** -13
 
 BANDS = [(0.0, 0.5), (0.5, 1.0), (1.0, 2.0), (2.0, 4.0), (4.0, np.inf)]
@@ -188,7 +192,7 @@ def assert_partials_close(m, l, acc, m_ref, l_ref, acc_ref, acc_abs, weight, wha
     """Split partials (m natural-log max, l sum of exponentials, acc unnormalised output)
     against the oracle's: m within 1e-4 (relative, at least 1e-4 absolute), l within 1e-4
     relative, and acc = sum_j p_j v_j within (u_w + 2^-13) * sum_j p_j |v_j| (each PV
-    weight rounded once to the MMA operand type, the rest fp32; ``acc_abs`` is the
+    weight carried as two MMA operands, see the module docstring; ``acc_abs`` is the
     oracle's acc over |V|, same split partition and maximum; ``abs_floor``: the int8
     subnormal-weight term, ``subnormal_floor``).  Empty splits: m = -inf, l = 0."""
     m, l, acc = (np.asarray(t, np.float64) for t in (m, l, acc))
