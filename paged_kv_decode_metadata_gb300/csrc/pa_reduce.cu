@@ -54,16 +54,21 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceParams p) 
   }
   const float* m = p.m + r * S;
   const float* l = p.l + r * S;
-  float mx = -CUDART_INF_F;
-  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, m[s]);
+  // the split maxima and sums of a lane's first (usually only) split slot are loaded
+  // together, so the sums cost no second round trip after the maximum is known
+  const float m0 = lane < S ? m[lane] : -CUDART_INF_F;
+  const float l0 = lane < S ? l[lane] : 0.f;
+  float mx = m0;
+  for (int s = lane + 32; s < S; s += 32) mx = fmaxf(mx, m[s]);
   mx = warp_max(mx);
   float total = 0.f;
   if (mx != -CUDART_INF_F) {
     for (int s = lane; s < S; s += 32) {
-      const float ms = m[s];
+      const float ms = s == lane ? m0 : m[s];
+      const float ls = s == lane ? l0 : l[s];
       const float ws = ms == -CUDART_INF_F ? 0.f : expf(ms - mx);
       w[s] = ws;
-      if (ws != 0.f) total += ws * l[s];
+      if (ws != 0.f) total += ws * ls;
     }
     total = warp_sum(total);
   }

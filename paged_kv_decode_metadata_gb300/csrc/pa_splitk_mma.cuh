@@ -12,16 +12,18 @@
 // (G = 4 bf16).  One m16n8k16 MMA does 2048 multiply-adds per warp instruction.
 //
 // GB300 mapping
-//   * CTA = 4 consumer warps + 1 producer warp.  The producer warp's lane 0 streams
+//   * CTA = 4 consumer warps (4 * NG for small grids) + 1 producer warp.  The producer warp's lane 0 streams
 //     64-token chunks with 4-D TMA tiled copies (cp.async.bulk.tensor) of the
 //     [num_pages, Hkv, page_size, 128] pools into a STAGES-deep ring; full/empty
 //     mbarriers hand stages back and forth, so there is no CTA-wide barrier per chunk.
 //     128-byte swizzle makes every ldmatrix / 16-byte shared load conflict free.
 //     Grids of at most one block per SM take a deeper ring at one CTA per SM.
-//   * Consumer warp w owns tokens [16w, 16w+16) of every chunk and keeps its own
-//     online-softmax state for its tokens; the four states are merged once at the end
-//     of the split (the same log-sum-exp combination the reducer applies across
-//     splits).  The weights of a column are relative to a reference maximum that moves
+//   * Consumer warps come in groups of four; warp w of a group owns tokens [16w, 16w+16)
+//     of each of its group's chunks and keeps its own online-softmax state for its
+//     tokens; the warps' states are merged once at the end of the split (the same
+//     log-sum-exp combination the reducer applies across splits).  One group consumes
+//     every chunk; grids of at most one block per SM use several groups, each taking
+//     every NG-th chunk, so a short split's chunks are worked on at once.  The weights of a column are relative to a reference maximum that moves
 //     only when a score passes it by more than 2^kMaxSlack (log2 units), so most slices
 //     need one warp vote instead of a shuffle reduction and a rescale.
 //   * Transposed orientation: S^T = K Q^T with M = 16 tokens, N = 8 columns (a column is
@@ -64,8 +66,12 @@ namespace pa {
 namespace mma {
 
 constexpr int kChunk = 64;
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// Consumer warps come in groups of four; a group shares the 64 tokens of a chunk (16
+// each).  One group (NG = 1) consumes every chunk; with NG groups, group g consumes the
+// chunks c with c % NG == g, so NG chunks are worked on at once (small grids).
+constexpr int kGroupWarps = 4;
+template <int NG>
+constexpr int threads_of() { return (NG * kGroupWarps + 1) * 32; }
 constexpr int kMaxSplitPages = 256;
 // Online-softmax slack (log2 units): the reference maximum of a column moves only when a
 // score exceeds it by more than this, so softmax weights stay below 2^8.
@@ -94,7 +100,7 @@ constexpr int kBiasPeriod = 16;
 #define PA_P_SPLIT 1
 #endif
 
-template <bool kQuant, int STAGES>
+template <bool kQuant, int STAGES, int NW>
 struct Layout {
   static constexpr int KV_BYTES = kQuant ? kChunk * 128 : kChunk * 256;  // per tensor per chunk
   static constexpr int SCALE_BYTES = kQuant ? kChunk * 4 : 0;
@@ -103,11 +109,11 @@ struct Layout {
   static constexpr int OFF_PAGES = STAGES * STAGE_BYTES;
   static constexpr int OFF_FULL = OFF_PAGES + kMaxSplitPages * 4;
   static constexpr int OFF_EMPTY = OFF_FULL + STAGES * 8;
-  static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;      // [4 warps][16 columns][3]
-  static constexpr int OFF_MISC = OFF_ML + kConsumerWarps * 16 * 3 * 4;  // abort, issued, done
+  static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;      // [NW warps][16 columns][3]
+  static constexpr int OFF_MISC = OFF_ML + NW * 16 * 3 * 4;  // abort, issued, done
   static constexpr int OFF_SKIP = OFF_MISC + 16;  // per stage: mask of its skipped pages
   static constexpr int SMEM = OFF_SKIP + (STAGES * 4 + 15) / 16 * 16 + 1024;  // + alignment slack
-  static constexpr int RED_BYTES = kConsumerWarps * 16 * 128 * 4;           // output merge buffer
+  static constexpr int RED_BYTES = NW * 16 * 128 * 4;           // output merge buffer
   static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "merge buffer reuses the ring");
 };
 
@@ -164,8 +170,9 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
+template <int NW>
 __device__ __forceinline__ void consumer_barrier() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
 }
 
 // Two bf16/fp16 values packed low-first.
@@ -285,11 +292,14 @@ __device__ __forceinline__ int64_t column_slot(int q_begin, int col, int G, int 
 
 // kWindow: the sliding-window variant (prm.window > 0); without it every window test
 // folds away at compile time.
-template <bool kQuant, int P, int STAGES, int MINB, int kNT, bool kWindow>
-__global__ void __launch_bounds__(kThreads, MINB)
+template <bool kQuant, int P, int STAGES, int MINB, int kNT, bool kWindow, int NG>
+__global__ void __launch_bounds__(threads_of<NG>(), MINB)
     splitk_mma_kernel(const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const SplitKParams prm) {
-  using L = Layout<kQuant, STAGES>;
+  static_assert(STAGES % NG == 0, "every group owns whole stages");
+  constexpr int kConsumerWarps = NG * kGroupWarps;
+  constexpr int kThreads = threads_of<NG>();
+  using L = Layout<kQuant, STAGES, kConsumerWarps>;
   constexpr bool kF16 = kQuant;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], kGroupWarps);
     }
     *abort_flag = 0;
     *issued_s = 0;
@@ -565,7 +575,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
     t_max[nt][0] = t_max[nt][1] = -CUDART_INF_F;
     l_part[nt][0] = l_part[nt][1] = 0.f;
   }
-  const int t0 = warp * 16;  // this warp's tokens inside every chunk
+  const int group = warp / kGroupWarps;
+  const int t0 = (warp % kGroupWarps) * 16;  // this warp's tokens inside its group's chunks
   bool failed = false;
   // Causal limit of this thread's columns, in token positions of the split: query i of a
   // request with q_len queries sees positions < n - q_len + i + 1 (its own token is the
@@ -583,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   // lim = n - tok_begin), relative to the split.
   const int lo_hi = window > 0 ? n - window - tok_begin : INT_MIN;
 
-  for (int c = 0; c < n_chunks; ++c) {
+  for (int c = group; c < n_chunks; c += NG) {
     const int stage = c % STAGES;
     if (!mbar_wait_bounded(&full[stage], static_cast<uint32_t>(c / STAGES) & 1u) || *abort_flag) {
       if (lane == 0) {
@@ -877,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
   trigger_dependents();
 
-  // ---- merge the four warps' softmax states, write the split's partials -------------
+  // ---- merge the consumer warps' softmax states, write the split's partials --------
   // Per column: M = the split's true maximum (over warps of the lane-reduced t_max);
   // warp w's weights are relative to its reference m_w <= M, so its sum and output
   // are scaled by 2^(m_w - M).
@@ -906,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         ml_s[(warp * 16 + head) * 3 + 2] = t_max[nt][e];
       }
   }
-  consumer_barrier();
+  consumer_barrier<kConsumerWarps>();
   if (failed || *abort_flag) {
     // Drain what the TMA warp issued so no copy lands after the CTA exits.  It may
     // first sit out its own bounded wait on a stage the consumers never released.
@@ -921,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
     return;
   }
-  float* red = reinterpret_cast<float*>(smem);  // [4 warps][16 heads][128 channels]
+  float* red = reinterpret_cast<float*>(smem);  // [warps][16 columns][128 channels]
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
@@ -948,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
       }
     }
-  consumer_barrier();
+  consumer_barrier<kConsumerWarps>();
   for (int idx = tid; idx < ncols * 32; idx += kConsumerWarps * 32) {
     const int head = idx >> 5, d = (idx & 31) * 4;  // column, channel
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1023,12 +1034,13 @@ inline cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, bool quan
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool kQuant, int P, int STAGES, int MINB, int kNT, bool kWindow>
+template <bool kQuant, int P, int STAGES, int MINB, int kNT, bool kWindow, int NG = 1>
 cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
                            dim3 grid, cudaStream_t stream, bool use_pdl) {
-  using L = Layout<kQuant, STAGES>;
+  using L = Layout<kQuant, STAGES, NG * kGroupWarps>;
+  constexpr int kThreads = threads_of<NG>();
   void (*kernel)(const CUtensorMap, const CUtensorMap, const SplitKParams) =
-      splitk_mma_kernel<kQuant, P, STAGES, MINB, kNT, kWindow>;
+      splitk_mma_kernel<kQuant, P, STAGES, MINB, kNT, kWindow, NG>;
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1047,9 +1059,9 @@ cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const C
 // (STAGES, MINB) for G <= 8 (one n-tile of heads) and for G = 16 (two n-tiles, more
 // registers per thread).
 // STAGES_DEEP > 0: grids of at most p.sm_count blocks with one n-tile use STAGES_DEEP
-// stages and one CTA per SM.
+// stages, GROUPS_DEEP consumer groups (chunks worked on at once) and one CTA per SM.
 template <bool kQuant, int STAGES1, int MINB1, int STAGES2, int MINB2, int STAGES_DEEP,
-          bool kWindow>
+          bool kWindow, int GROUPS_DEEP = 1>
 cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_size,
                             cudaStream_t stream, bool use_pdl) {
   CUtensorMap mk, mv;
@@ -1066,8 +1078,8 @@ cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_s
   if (page_size == PP) {                                                                       \
     if constexpr (STAGES_DEEP > 0) {                                                           \
       if (deep)                                                                                \
-        return launch_mma_one<kQuant, PP, (STAGES_DEEP > 0 ? STAGES_DEEP : 1), 1, 1, kWindow>( \
-            p, mk, mv, grid, stream, use_pdl);                                                 \
+        return launch_mma_one<kQuant, PP, (STAGES_DEEP > 0 ? STAGES_DEEP : GROUPS_DEEP), 1, 1, \
+                              kWindow, GROUPS_DEEP>(p, mk, mv, grid, stream, use_pdl);           \
     }                                                                                          \
     return two_tiles                                                                           \
                ? launch_mma_one<kQuant, PP, STAGES2, MINB2, 2, kWindow>(p, mk, mv, grid, stream,  \

@@ -45,3 +45,11 @@
 #ifndef PA_MMA_INT8_STAGES_DEEP
 #define PA_MMA_INT8_STAGES_DEEP 8
 #endif
+// Consumer groups of four warps in that configuration: each takes every GROUPS-th chunk
+// (its own stages of the ring), so GROUPS chunks of a short split are worked on at once.
+#ifndef PA_MMA_BF16_GROUPS_DEEP
+#define PA_MMA_BF16_GROUPS_DEEP 2
+#endif
+#ifndef PA_MMA_INT8_GROUPS_DEEP
+#define PA_MMA_INT8_GROUPS_DEEP 2
+#endif
