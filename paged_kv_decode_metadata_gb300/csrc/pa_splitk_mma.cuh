@@ -596,7 +596,9 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
 
   for (int c = group; c < n_chunks; c += NG) {
     const int stage = c % STAGES;
-    if (!mbar_wait_bounded(&full[stage], static_cast<uint32_t>(c / STAGES) & 1u) || *abort_flag) {
+    // (a TMA warp that stopped issuing leaves this wait to run out; the consumers do
+    // not poll the abort flag on every chunk)
+    if (!mbar_wait_bounded(&full[stage], static_cast<uint32_t>(c / STAGES) & 1u)) {
       if (lane == 0) {
         record_error(prm.err, kErrWaitTimeout);
         *abort_flag = 1;
