@@ -198,6 +198,14 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz.f32: relative error ~2^-22,
+// results below 2^-126 flush to 0, 2^-inf = 0): the softmax weights of the inner loop.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Power of two 2^e with e clamped to [-100, 100] (exact; built from the exponent bits).
 __device__ __forceinline__ float pow2_clamped(int e) {
   e = max(-100, min(100, e));
@@ -563,17 +571,20 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
   // two that puts the largest V scale seen so far in [64, 128): weights stay below
   // 2^kMaxSlack * 128 (no fp16 overflow) and every weight within 2^-20 of the largest
   // one is a normal fp16 number (no subnormal rounding).  o and wsum are in those units;
-  // vmul only shrinks (exact rescale) when a larger scale appears.  0: not set yet.
-  float vmul = 0.f;
+  // vmul only shrinks (exact rescale) when a larger scale appears; it starts at 2^100,
+  // so the first slice with a nonzero scale sets it.
+  float vmul = 0x1p100f;
   // softmax state of heads 8*nt + 2*tig + e (identical in the 8 lanes sharing tig)
   // m_run: the reference maximum the weights are relative to (warp-uniform per column);
   // t_max: this thread's true maximum of its own scores, reduced once per split.
-  float m_run[kNT][2], l_part[kNT][2], t_max[kNT][2];
+  // ref: m_run, or 0 while a column has no score yet (its scores are all -inf then)
+  float m_run[kNT][2], l_part[kNT][2], t_max[kNT][2], ref[kNT][2];
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) {
     m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
     t_max[nt][0] = t_max[nt][1] = -CUDART_INF_F;
     l_part[nt][0] = l_part[nt][1] = 0.f;
+    ref[nt][0] = ref[nt][1] = 0.f;
   }
   const int group = warp / kGroupWarps;
   const int t0 = (warp % kGroupWarps) * 16;  // this warp's tokens inside its group's chunks
@@ -686,13 +697,13 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
         vs_a = tok_a < valid ? vscale[tok_a] : 0.f;
         vs_b = tok_b < valid ? vscale[tok_b] : 0.f;
         const float vhi = fmaxf(vs_a, vs_b);
-        if (__any_sync(0xffffffffu, vmul == 0.f || vhi * vmul >= 128.f)) {
+        if (__any_sync(0xffffffffu, vhi * vmul >= 128.f)) {
           float vmax = vhi;  // over the warp's 16 tokens
 #pragma unroll
           for (int m = 4; m <= 16; m <<= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, m));
           if (vmax > 0.f) {
             const float vmul_new = pow2_clamped(6 - float_exponent(vmax));
-            if (vmul != 0.f && vmul_new < vmul) {
+            if (vmul_new < vmul) {
               const float r = vmul_new / vmul;  // a power of two: exact
 #pragma unroll
               for (int nt = 0; nt < kNT; ++nt) {
@@ -704,7 +715,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
                 for (int r4 = 0; r4 < 4; ++r4) wsum[nt][r4] *= r;
               }
             }
-            if (vmul == 0.f || vmul_new < vmul) vmul = vmul_new;
+            if (vmul_new < vmul) vmul = vmul_new;
           }
         }
         vs_a *= vmul;
@@ -752,8 +763,9 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
           for (int e = 0; e < 2; ++e) {
             const float m_new = fmaxf(m_run[nt][e], e == 0 ? mx0 : mx1);
             if (m_new != -CUDART_INF_F) {
-              alpha[e] = exp2f(m_run[nt][e] - m_new);
+              alpha[e] = fast_exp2(m_run[nt][e] - m_new);
               m_run[nt][e] = m_new;
+              ref[nt][e] = m_new;
             }
           }
           if (alpha[0] != 1.f || alpha[1] != 1.f) {
@@ -774,10 +786,8 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
         }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          // a column with no score yet (reference -inf) has only -inf scores here
-          const float ref = m_run[nt][e] == -CUDART_INF_F ? 0.f : m_run[nt][e];
-          p[e] = exp2f(x[e] - ref);
-          p[2 + e] = exp2f(x[2 + e] - ref);
+          p[e] = fast_exp2(x[e] - ref[nt][e]);
+          p[2 + e] = fast_exp2(x[2 + e] - ref[nt][e]);
           l_part[nt][e] = l_part[nt][e] * alpha[e] + (p[e] + p[2 + e]);
         }
         // P^T as the B operand of O^T += V^T P^T: transpose the two 8x8 (token, head)
@@ -945,7 +955,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + head) * 3 + 2]);
         float scale = m_run[nt][e] == -CUDART_INF_F ? 0.f : exp2f(m_run[nt][e] - mrow);
-        if constexpr (kQuant) scale = vmul > 0.f ? scale / vmul : 0.f;  // vmul: power of two
+        if constexpr (kQuant) scale /= vmul;  // vmul: a power of two
         float* dst = red + (warp * 16 + head) * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
