@@ -38,6 +38,14 @@ PA_API pa_status pa_set_timestamp_buffer(uint64_t* buffer);
  */
 PA_API pa_status pa_set_test_hold_loads(int32_t hold);
 
+/*
+ * A/B test hook: with off != 0, later producer launches keep one block per (request,
+ * kv head, split) even where the library would run its persistent form (one CTA per
+ * resident slot claiming items of a largest-first work list); off = 0 restores the
+ * library's choice.  Both forms give the same bits.
+ */
+PA_API pa_status pa_set_test_no_persist(int32_t off);
+
 #ifdef __cplusplus
 }
 #endif

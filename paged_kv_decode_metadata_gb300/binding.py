@@ -78,6 +78,8 @@ def load_instrumented() -> ctypes.CDLL:
             lib.pa_set_timestamp_buffer.restype = ctypes.c_int
             lib.pa_set_test_hold_loads.argtypes = [ctypes.c_int32]
             lib.pa_set_test_hold_loads.restype = ctypes.c_int
+            lib.pa_set_test_no_persist.argtypes = [ctypes.c_int32]
+            lib.pa_set_test_no_persist.restype = ctypes.c_int
             _ts_lib = lib
     return _ts_lib
 

@@ -41,6 +41,8 @@ std::atomic<int32_t> g_producer{PA_PRODUCER_AUTO};
 std::atomic<unsigned long long*> g_ts{nullptr};
 // Instrumented build: non-zero makes later producer launches issue no copies.
 std::atomic<int32_t> g_hold_loads{0};
+// Instrumented build: non-zero keeps later producer launches at one block per item.
+std::atomic<int32_t> g_no_persist{0};
 std::atomic<int> g_sm_count[kMaxDevices];
 
 cudaError_t error_word(unsigned int** out) {
@@ -293,8 +295,10 @@ pa_status decode_splitk_impl(const void* q, const void* k_cache, const void* v_c
   p.max_seq_pages = max_seq_pages;
   p.pages_per_split = static_cast<int32_t>(cdiv(split_pages, num_splits));
   p.window = window;
+  p.bs = bs;
   p.sm_count = sm_count_of_current_device();
   p.hold_loads = g_hold_loads.load();
+  p.no_persist = g_no_persist.load();
   p.num_splits = num_splits;
   p.q_scale = sm_scale * 1.4426950408889634f;  // log2(e): the kernel works in base 2
   p.cu_seqlens_q = cu_seqlens_q;
@@ -709,6 +713,11 @@ pa_status pa_set_timestamp_buffer(uint64_t* buffer) {
 
 pa_status pa_set_test_hold_loads(int32_t hold) {
   g_hold_loads.store(hold != 0 ? 1 : 0);
+  return PA_OK;
+}
+
+pa_status pa_set_test_no_persist(int32_t off) {
+  g_no_persist.store(off != 0 ? 1 : 0);
   return PA_OK;
 }
 #endif

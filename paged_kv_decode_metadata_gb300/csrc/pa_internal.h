@@ -65,9 +65,12 @@ struct SplitKParams {
   // request's first visible position, and skips pages whose table entry is -1.
   // pages_per_split is then counted over the window's pages.  0: whole context.
   int32_t window;
+  int32_t bs;        // requests (the persistent form walks them itself)
+  int32_t work_slot;  // persistent form: the work-claim counter this launch uses
   int32_t sm_count;  // SMs of the device (grids of at most this many blocks take the
                      // deep-pipeline configuration)
   int32_t hold_loads;  // instrumented build only: the TMA warp issues nothing (timeout test)
+  int32_t no_persist;  // instrumented build only: one block per item (A/B test)
   float* m_out;
   float* l_out;
   float* acc_out;

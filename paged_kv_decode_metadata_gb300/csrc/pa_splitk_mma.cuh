@@ -73,6 +73,17 @@ constexpr int kGroupWarps = 4;
 template <int NG>
 constexpr int threads_of() { return (NG * kGroupWarps + 1) * 32; }
 constexpr int kMaxSplitPages = 256;
+// The persistent form (one CTA per resident slot walking a work list) takes batches of
+// at most this many requests.
+constexpr int kMaxPersistRequests = 128;
+// Work-claim counters of the persistent form: [claimed items, CTAs done] per slot.  A
+// launch takes the next slot (host side, round robin); its last CTA to finish sets the
+// slot back to zero, so the slot is ready for its next launch.  Launches of one stream
+// never overlap their claims (each waits for the previous producer to complete), so
+// only more than kWorkSlots producers in flight on different streams could collide.
+constexpr int kWorkSlots = 64;
+static __device__ unsigned int g_work_claims[kWorkSlots][2];
+static std::atomic<unsigned int> g_next_work_slot{0};
 // Online-softmax slack (log2 units): the reference maximum of a column moves only when a
 // score exceeds it by more than this, so softmax weights stay below 2^8.
 #ifndef PA_MAX_SLACK
@@ -112,9 +123,14 @@ struct Layout {
   static constexpr int OFF_ML = OFF_EMPTY + STAGES * 8;      // [NW warps][16 columns][3]
   static constexpr int OFF_MISC = OFF_ML + NW * 16 * 3 * 4;  // abort, issued, done
   static constexpr int OFF_SKIP = OFF_MISC + 16;  // per stage: mask of its skipped pages
-  static constexpr int SMEM = OFF_SKIP + (STAGES * 4 + 15) / 16 * 16 + 1024;  // + alignment slack
-  static constexpr int RED_BYTES = NW * 16 * 128 * 4;           // output merge buffer
-  static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "merge buffer reuses the ring");
+  // persistent form: per-request length, full and partial split counts, the requests
+  // ranked by partial-split size, prefix of full splits (+1), two counts
+  // persistent form: per stage, the work-list position of the item whose first chunk
+  // the stage holds (-1: no more work)
+  static constexpr int OFF_DESC = OFF_SKIP + (STAGES * 4 + 15) / 16 * 16;
+  static constexpr int OFF_SCHED = OFF_DESC + (STAGES * 4 + 15) / 16 * 16;
+  static constexpr int SCHED_INTS = 5 * kMaxPersistRequests + 3;
+  static constexpr int SMEM = OFF_SCHED + (SCHED_INTS * 4 + 15) / 16 * 16 + 1024;  // + align slack
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -300,21 +316,35 @@ __device__ __forceinline__ int64_t column_slot(int q_begin, int col, int G, int 
 
 // kWindow: the sliding-window variant (prm.window > 0); without it every window test
 // folds away at compile time.
-template <bool kQuant, int P, int STAGES, int MINB, int kNT, bool kWindow, int NG>
+// kPersist: the persistent form.  The grid is one CTA per resident slot; each CTA walks
+// a list of (request, kv head, split) items, built in shared memory from the request
+// lengths: the splits with a full page range first (all the same size), then the
+// partial last splits of each request, largest first, handed out in snake order over
+// the CTAs so that the slots finish together.  The ring keeps cycling across items, so
+// the TMA warp copies the next item's first chunks while the consumers finish the
+// current one (a fresh block would wait ~2 us for its first data).  One consumer group,
+// one query per request, at most kMaxPersistRequests requests.
+template <bool kQuant, int P, int STAGES, int MINB, int kNT, bool kWindow, int NG,
+          bool kPersist>
 __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     splitk_mma_kernel(const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const SplitKParams prm) {
   static_assert(STAGES % NG == 0, "every group owns whole stages");
+  static_assert(!kPersist || NG == 1, "the persistent form has one consumer group");
   constexpr int kConsumerWarps = NG * kGroupWarps;
   constexpr int kThreads = threads_of<NG>();
   using L = Layout<kQuant, STAGES, kConsumerWarps>;
+  // output merge buffer: [consumer warps][8 * kNT columns][128 channels] fp32; the
+  // persistent form merges in the stage of the item's last chunk (held until then)
+  constexpr int kRedBytes = kConsumerWarps * 8 * kNT * 128 * 4;
+  static_assert(kRedBytes <= STAGES * L::STAGE_BYTES, "merge buffer reuses the ring");
+  static_assert(!kPersist || kRedBytes <= L::STAGE_BYTES, "merge buffer fits one stage");
   constexpr bool kF16 = kQuant;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t smem_base = smem_addr(smem);
 
-  const int split = blockIdx.x, kvh = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int G = prm.num_q_heads / prm.num_kv_heads;
@@ -356,14 +386,14 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
 
   // ---- consumers: Q^T fragments in registers, independent of the metadata stage -----
   // (with several queries per request their rows come from cu_seqlens_q, a metadata
-  // output, so Q is loaded after the wait instead).  The TMA warp does not wait for
-  // this: it goes straight to the split's length and page indices and starts copying.
-  const int b = blockIdx.z;
+  // output, and the persistent form learns its items from the lengths, so Q is loaded
+  // after the wait instead).  The TMA warp does not wait for this: it goes straight to
+  // the split's length and page indices and starts copying.
   const bool multi = prm.cu_seqlens_q != nullptr;
   uint32_t qb[kNT][8][2];
   float kbias[kNT][2], qf[kNT][2];
-  if (!multi && is_consumer)
-    load_q_fragments<kF16, kNT>(prm, b, 1, kvh, G, gid, tig, qb, kbias, qf);
+  if (!kPersist && !multi && is_consumer)
+    load_q_fragments<kF16, kNT>(prm, blockIdx.z, 1, blockIdx.y, G, gid, tig, qb, kbias, qf);
 
   // ---- everything below reads what the metadata stage wrote -------------------------
   grid_dependency_wait();
@@ -371,6 +401,141 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
   if (prm.ts != nullptr && tid == kConsumerWarps * 32)
     atomicMin(prm.ts + 3 * 1 + kTsReady, global_timer_ns());
 #endif
+  const int window = kWindow ? prm.window : 0;
+  const int cap = prm.max_seq_pages * P;
+  const int pps = prm.pages_per_split;
+  const int Hkv = prm.num_kv_heads;
+
+  // ---- persistent form: the work list ------------------------------------------------
+  int* n_s = reinterpret_cast<int*>(smem + L::OFF_SCHED);  // clamped request lengths
+  int* full_s = n_s + kMaxPersistRequests;                  // splits with a full range
+  int* part_s = full_s + kMaxPersistRequests;               // pages of the partial split
+  int* part_list = part_s + kMaxPersistRequests;            // requests by partial size
+  int* pref_s = part_list + kMaxPersistRequests;            // exclusive prefix of full_s
+  int* cnt_s = pref_s + kMaxPersistRequests + 1;            // [full splits, partials]
+  int total_items = 1;
+  if constexpr (kPersist) {
+    const int bs = prm.bs;
+    for (int r = tid; r < bs; r += kThreads) {
+      int n = prm.cache_seqlens[r];
+      if (n < 0 || n > cap) {
+        if (blockIdx.x == 0) record_error(prm.err, kErrSeqLenOutOfRange);
+        n = n < 0 ? 0 : cap;
+      }
+      // the split partition of a request: from its first visible page (window) or page 0
+      const int base = window > 0 ? max(0, n - window) / P : 0;
+      const int pages = max(0, (n + P - 1) / P - base);
+      const int fulls = min(pages / pps, S);
+      n_s[r] = n;
+      full_s[r] = fulls;
+      part_s[r] = fulls < S ? pages - fulls * pps : 0;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0, partials = 0;
+      for (int r0 = 0; r0 < bs; r0 += 32) {
+        const int r = r0 + lane;
+        const int v = r < bs ? full_s[r] : 0;
+        int incl = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int up = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += up;
+        }
+        if (r < bs) pref_s[r] = carry + incl - v;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+        partials += __popc(__ballot_sync(0xffffffffu, r < bs && part_s[r] > 0));
+      }
+      if (lane == 0) {
+        pref_s[bs] = carry;
+        cnt_s[0] = carry;
+        cnt_s[1] = partials;
+      }
+    }
+    // rank of each partial split: larger first, ties by request index
+    for (int r = tid; r < bs; r += kThreads) {
+      const int pr = part_s[r];
+      if (pr > 0) {
+        int rank = 0;
+        for (int q = 0; q < bs; ++q) {
+          const int pq = part_s[q];
+          rank += (pq > pr || (pq == pr && q < r)) ? 1 : 0;
+        }
+        part_list[rank] = r;
+      }
+    }
+    __syncthreads();
+    total_items = (cnt_s[0] + cnt_s[1]) * Hkv;
+  }
+  // Item at position `pos` of the persistent form's work list: the splits with a full
+  // page range (kv head fastest), then the partial splits by size, largest first.
+  auto decode_item = [&](int pos, int& b_, int& kvh_, int& split_) {
+    const int full_items = cnt_s[0] * Hkv;
+    if (pos < full_items) {
+      const int f = pos / Hkv;
+      kvh_ = pos - f * Hkv;
+      int lo = 0, hi = prm.bs;  // the request whose full splits hold the f-th one
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pref_s[mid] <= f) lo = mid; else hi = mid;
+      }
+      b_ = lo;
+      split_ = f - pref_s[lo];
+    } else {
+      const int k2 = pos - full_items;
+      const int rank = k2 / Hkv;
+      kvh_ = k2 - rank * Hkv;
+      b_ = part_list[rank];
+      split_ = full_s[b_];
+    }
+  };
+  // Persistent form: items are claimed one at a time by the TMA warp from this launch's
+  // counter (the work list is largest first, so free CTAs take the largest items left);
+  // the position of each item travels to the consumers in the descriptor of the stage
+  // that holds its first chunk.
+  unsigned int* claims = kPersist ? g_work_claims[prm.work_slot] : nullptr;
+  int32_t* desc_s = reinterpret_cast<int32_t*>(smem + L::OFF_DESC);
+
+  // ring position: chunks this thread's role has issued (TMA warp) or consumed so far
+  int gc = 0;
+  bool failed = false, triggered = false;
+  for (int round = 0;; ++round) {
+  int b, kvh, split;
+  int item_pos = 0;  // persistent form: the item's position in the work list
+  if constexpr (kPersist) {
+    int pos = -1;
+    if (!is_consumer) {  // claim the next item of the work list
+      if (lane == 0 && !*abort_flag) pos = static_cast<int>(atomicAdd(claims, 1u));
+      pos = __shfl_sync(0xffffffffu, pos, 0);
+      if (pos < 0 || pos >= total_items) break;
+    } else {  // learn it from the descriptor of the stage holding its first chunk
+      const int stage0 = gc % STAGES;
+      if (!mbar_wait_bounded(&full[stage0], static_cast<uint32_t>(gc / STAGES) & 1u) &&
+          lane == 0) {
+        record_error(prm.err, kErrWaitTimeout);
+        *abort_flag = 1;
+      }
+      consumer_barrier<kConsumerWarps>();  // every consumer warp takes the same path
+      if (*abort_flag) {
+        failed = true;
+        break;
+      }
+      pos = desc_s[stage0];
+      if (pos < 0) break;  // no more work
+    }
+    decode_item(pos, b, kvh, split);
+    item_pos = pos;
+    // the consumers load this item's Q rows once its first chunk has landed: bring them
+    // into L2 now, while the ring still holds the previous item
+    if (!is_consumer && lane < 2 * G)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(prm.q) +
+                   (static_cast<int64_t>(b) * prm.num_q_heads + kvh * G) * 256 + lane * 128));
+  } else {
+    if (round > 0) break;
+    b = blockIdx.z;
+    kvh = blockIdx.y;
+    split = blockIdx.x;
+  }
 
   int q_begin = b, q_len = 1;
   if (multi) {
@@ -382,6 +547,8 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     }
     if (is_consumer)
       load_q_fragments<kF16, kNT>(prm, q_begin, q_len, kvh, G, gid, tig, qb, kbias, qf);
+  } else if (kPersist && is_consumer) {
+    load_q_fragments<kF16, kNT>(prm, b, 1, kvh, G, gid, tig, qb, kbias, qf);
   }
   const int ncols = q_len * G;  // (query, head) columns of this request and kv head
 
@@ -390,8 +557,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
   // bounds-checked where they are used).  With a window the split starts at the page of
   // the request's first visible position, which depends on the length.  Only the TMA
   // warp reads the page indices.
-  const int window = kWindow ? prm.window : 0;
-  int p_begin = split * prm.pages_per_split;
+  int p_begin = split * pps;
   const int32_t* pt_row = prm.page_table + static_cast<int64_t>(b) * prm.page_table_stride;
   auto cache_page_indices = [&]() {
     pt_row += p_begin;
@@ -400,11 +566,15 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     for (int i = lane; i < pages_cap; i += 32) pages_s[i] = pt_row[i];
   };
   if (window == 0 && !is_consumer) cache_page_indices();
-  int n = prm.cache_seqlens[b];
-  const int cap = prm.max_seq_pages * P;
-  if (n < 0 || n > cap) {
-    if (tid == 0 && split == 0 && kvh == 0) record_error(prm.err, kErrSeqLenOutOfRange);
-    n = n < 0 ? 0 : cap;
+  int n;
+  if constexpr (kPersist) {
+    n = n_s[b];
+  } else {
+    n = prm.cache_seqlens[b];
+    if (n < 0 || n > cap) {
+      if (tid == 0 && split == 0 && kvh == 0) record_error(prm.err, kErrSeqLenOutOfRange);
+      n = n < 0 ? 0 : cap;
+    }
   }
   if (window > 0) {
     p_begin += max(0, n - q_len - window + 1) / P;
@@ -415,7 +585,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
   const int tok_begin = p_begin * P;
   const int n_tok = min(p_end * P, n) - tok_begin;
 
-  if (n_tok <= 0) {
+  if (n_tok <= 0) {  // (never an item of the persistent form's work list)
     trigger_dependents();
     if (tid < ncols) {
       const int64_t slot = column_slot(q_begin, tid, G, kvh, prm.num_q_heads, S, split);
@@ -445,16 +615,20 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     if (lane == 0) {
       const uint64_t policy = l2_evict_first_policy();
       for (int c = 0; c < n_chunks; ++c) {
-        const int stage = c % STAGES;
-        if (c >= STAGES) {
-          const uint32_t parity = static_cast<uint32_t>(c / STAGES - 1) & 1u;
+        const int g = gc + c;  // ring position of this chunk
+        const int stage = g % STAGES;
+        if (g >= STAGES) {
+          const uint32_t parity = static_cast<uint32_t>(g / STAGES - 1) & 1u;
           if (!mbar_wait_bounded(&empty[stage], parity) || *abort_flag) {
             record_error(prm.err, kErrWaitTimeout);
             *abort_flag = 1;
             break;
           }
         }
-        *issued_s = c + 1;
+        *issued_s = g + 1;
+        // the first chunk's stage carries the item to the consumers (published by the
+        // arrive on its full barrier below, read after their wait on it)
+        if (kPersist && c == 0) desc_s[stage] = item_pos;
         const uint32_t kdst = smem_base + stage * L::STAGE_BYTES;
         const uint32_t vdst = kdst + L::KV_BYTES;
         const int ctok = c * kChunk;
@@ -544,13 +718,11 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
           }
         }
       }
-      // stopped early: the consumers have given up, so nothing else waits for these
-      if (*abort_flag) drain_issued(*issued_s);
-      __threadfence_block();
-      *producer_done = 1;
     }
-    trigger_dependents();
-    return;
+    __syncwarp();  // lane 0 is done with this item's page indices
+    gc += n_chunks;
+    if (*abort_flag) break;
+    continue;
   }
 
   // ======================= consumer warps =============================================
@@ -588,7 +760,6 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
   }
   const int group = warp / kGroupWarps;
   const int t0 = (warp % kGroupWarps) * 16;  // this warp's tokens inside its group's chunks
-  bool failed = false;
   // Causal limit of this thread's columns, in token positions of the split: query i of a
   // request with q_len queries sees positions < n - q_len + i + 1 (its own token is the
   // request's (q_len - i)-th newest).  One query per request: the whole context.
@@ -606,10 +777,11 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
   const int lo_hi = window > 0 ? n - window - tok_begin : INT_MIN;
 
   for (int c = group; c < n_chunks; c += NG) {
-    const int stage = c % STAGES;
+    const int g = gc + c;  // ring position of this chunk
+    const int stage = g % STAGES;
     // (a TMA warp that stopped issuing leaves this wait to run out; the consumers do
     // not poll the abort flag on every chunk)
-    if (!mbar_wait_bounded(&full[stage], static_cast<uint32_t>(c / STAGES) & 1u)) {
+    if (!mbar_wait_bounded(&full[stage], static_cast<uint32_t>(g / STAGES) & 1u)) {
       if (lane == 0) {
         record_error(prm.err, kErrWaitTimeout);
         *abort_flag = 1;
@@ -882,7 +1054,8 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     // before the TMA (async proxy) refills the buffer
     if (!kQuant && active && partial) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
+    // (the persistent form keeps the item's last stage for the merge below)
+    if (lane == 0 && !(kPersist && c == n_chunks - 1)) mbar_arrive(&empty[stage]);
     if constexpr (kVBias) {
       if (c % kBiasPeriod == kBiasPeriod - 1) {
 #pragma unroll
@@ -898,7 +1071,10 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     }
   }
 
-  trigger_dependents();
+  if (!kPersist) {  // (the persistent form signals once its CTA has no item left)
+    trigger_dependents();
+    triggered = true;
+  }
 
   // ---- merge the consumer warps' softmax states, write the split's partials --------
   // Per column: M = the split's true maximum (over warps of the lane-reduced t_max);
@@ -944,7 +1120,9 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     }
     return;
   }
-  float* red = reinterpret_cast<float*>(smem);  // [warps][16 columns][128 channels]
+  // [warps][8 * kNT columns][128 channels]: the ring (its start, or the held stage)
+  const int held_stage = (gc + n_chunks - 1) % STAGES;
+  float* red = reinterpret_cast<float*>(kPersist ? smem + held_stage * L::STAGE_BYTES : smem);
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
@@ -956,7 +1134,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
         for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + head) * 3 + 2]);
         float scale = m_run[nt][e] == -CUDART_INF_F ? 0.f : exp2f(m_run[nt][e] - mrow);
         if constexpr (kQuant) scale /= vmul;  // vmul: a power of two
-        float* dst = red + (warp * 16 + head) * 128;
+        float* dst = red + (warp * 8 * kNT + head) * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int ch0 = kQuant ? 16 * i + 2 * gid : 16 * i + gid;
@@ -977,7 +1155,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float4 v = *reinterpret_cast<const float4*>(red + (w * 16 + head) * 128 + d);
+      const float4 v = *reinterpret_cast<const float4*>(red + (w * 8 * kNT + head) * 128 + d);
       sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
     }
     *reinterpret_cast<float4*>(
@@ -997,6 +1175,77 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     prm.m_out[slot] = mrow * 0.69314718055994530942f;
     prm.l_out[slot] = lsum;
   }
+  if constexpr (kPersist) {
+    // every consumer has read the merge buffer and ml_s: hand the held stage back (the
+    // merge stores are generic-proxy writes the next TMA copy must be ordered after)
+    consumer_barrier<kConsumerWarps>();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) mbar_arrive(&empty[held_stage]);
+  }
+  gc += n_chunks;
+  }  // item loop
+
+  if (!is_consumer) {
+    if (lane == 0) {
+      if constexpr (kPersist) {
+        // no item left: a stage with descriptor -1 tells the consumers
+        if (!*abort_flag) {
+          const int stage = gc % STAGES;
+          if (gc >= STAGES &&
+              (!mbar_wait_bounded(&empty[stage], static_cast<uint32_t>(gc / STAGES - 1) & 1u) ||
+               *abort_flag)) {
+            record_error(prm.err, kErrWaitTimeout);
+            *abort_flag = 1;
+          } else {
+            desc_s[stage] = -1;
+            mbar_arrive(&full[stage]);
+          }
+        }
+        // this CTA claims nothing more; the last CTA to get here resets the counter
+        __threadfence();
+        if (atomicAdd(claims + 1, 1u) == gridDim.x - 1) {
+          claims[0] = 0;
+          claims[1] = 0;
+          __threadfence();
+        }
+      }
+      // stopped early: the consumers have given up, so nothing else waits for these
+      if (*abort_flag) drain_issued(*issued_s);
+      __threadfence_block();
+      *producer_done = 1;
+    }
+    trigger_dependents();
+    return;
+  }
+  if (kPersist && failed) {
+    // Drain what the TMA warp issued so no copy lands after the CTA exits (it may first
+    // sit out its own bounded wait on a stage the consumers never released).
+    if (tid == 0) {
+      const unsigned long long start = global_timer_ns();
+      while (*producer_done == 0 && global_timer_ns() - start < 2 * kWaitLimitNs) {
+      }
+      if (*producer_done != 0) {
+        __threadfence_block();
+        drain_issued(*issued_s);
+      }
+    }
+    return;
+  }
+  if constexpr (kPersist) {
+    // splits past a request's last page range: no tokens (m = -inf, l = 0); the
+    // (request, kv head) pairs are shared out over the CTAs
+    for (int pair = blockIdx.x; pair < prm.bs * Hkv; pair += gridDim.x) {
+      const int rb = pair / Hkv, rk = pair - rb * Hkv;
+      const int first = full_s[rb] + (part_s[rb] > 0 ? 1 : 0);
+      for (int t = tid; t < (S - first) * G; t += kConsumerWarps * 32) {
+        const int sp = first + t / G;
+        const int64_t slot = column_slot(rb, t % G, G, rk, prm.num_q_heads, S, sp);
+        prm.m_out[slot] = -CUDART_INF_F;
+        prm.l_out[slot] = 0.f;
+      }
+    }
+  }
+  if (!triggered) trigger_dependents();
   PA_TS_LAST(prm.ts, 1);
 }
 
@@ -1046,13 +1295,14 @@ inline cudaError_t encode_pool_map(CUtensorMap* map, const void* pool, bool quan
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <bool kQuant, int P, int STAGES, int MINB, int kNT, bool kWindow, int NG = 1>
+template <bool kQuant, int P, int STAGES, int MINB, int kNT, bool kWindow, int NG = 1,
+          bool kPersist = false>
 cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
                            dim3 grid, cudaStream_t stream, bool use_pdl) {
   using L = Layout<kQuant, STAGES, NG * kGroupWarps>;
   constexpr int kThreads = threads_of<NG>();
   void (*kernel)(const CUtensorMap, const CUtensorMap, const SplitKParams) =
-      splitk_mma_kernel<kQuant, P, STAGES, MINB, kNT, kWindow, NG>;
+      splitk_mma_kernel<kQuant, P, STAGES, MINB, kNT, kWindow, NG, kPersist>;
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1072,8 +1322,11 @@ cudaError_t launch_mma_one(const SplitKParams& p, const CUtensorMap& mk, const C
 // registers per thread).
 // STAGES_DEEP > 0: grids of at most p.sm_count blocks with one n-tile use STAGES_DEEP
 // stages, GROUPS_DEEP consumer groups (chunks worked on at once) and one CTA per SM.
+// PERSIST: grids of at least two blocks per resident slot (one n-tile, one query per
+// request, at most kMaxPersistRequests requests) run the persistent form, one CTA per
+// slot.
 template <bool kQuant, int STAGES1, int MINB1, int STAGES2, int MINB2, int STAGES_DEEP,
-          bool kWindow, int GROUPS_DEEP = 1>
+          bool kWindow, int GROUPS_DEEP = 1, bool PERSIST = false>
 cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_size,
                             cudaStream_t stream, bool use_pdl) {
   CUtensorMap mk, mv;
@@ -1084,14 +1337,27 @@ cudaError_t launch_mma_impl(const SplitKParams& p, int bs, int group, int page_s
   const dim3 grid(static_cast<unsigned>(p.num_splits), static_cast<unsigned>(p.num_kv_heads),
                   static_cast<unsigned>(bs));
   const bool two_tiles = group * (p.cu_seqlens_q != nullptr ? p.max_q_len : 1) > 8;
-  const bool deep = STAGES_DEEP > 0 && !two_tiles &&
-                    static_cast<int64_t>(grid.x) * grid.y * grid.z <= p.sm_count;
+  const int64_t blocks = static_cast<int64_t>(grid.x) * grid.y * grid.z;
+  const bool deep = STAGES_DEEP > 0 && !two_tiles && blocks <= p.sm_count;
+  const int64_t slots = static_cast<int64_t>(p.sm_count) * MINB1;
+  const bool persist = PERSIST && !two_tiles && !deep && p.cu_seqlens_q == nullptr &&
+                       bs <= kMaxPersistRequests && slots > 0 && blocks >= 2 * slots &&
+                       !p.no_persist;
+  const dim3 persist_grid(static_cast<unsigned>(persist ? slots : 1));
 #define PA_MMA_CASE(PP)                                                                        \
   if (page_size == PP) {                                                                       \
     if constexpr (STAGES_DEEP > 0) {                                                           \
       if (deep)                                                                                \
         return launch_mma_one<kQuant, PP, (STAGES_DEEP > 0 ? STAGES_DEEP : GROUPS_DEEP), 1, 1, \
                               kWindow, GROUPS_DEEP>(p, mk, mv, grid, stream, use_pdl);           \
+    }                                                                                          \
+    if constexpr (PERSIST) {                                                                   \
+      if (persist) {                                                                           \
+        SplitKParams pp = p;                                                                   \
+        pp.work_slot = static_cast<int32_t>(g_next_work_slot.fetch_add(1) % kWorkSlots);       \
+        return launch_mma_one<kQuant, PP, STAGES1, MINB1, 1, kWindow, 1, true>(                \
+            pp, mk, mv, persist_grid, stream, use_pdl);                                        \
+      }                                                                                        \
     }                                                                                          \
     return two_tiles                                                                           \
                ? launch_mma_one<kQuant, PP, STAGES2, MINB2, 2, kWindow>(p, mk, mv, grid, stream,  \

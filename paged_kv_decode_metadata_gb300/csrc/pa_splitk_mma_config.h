@@ -53,3 +53,20 @@
 #ifndef PA_MMA_INT8_GROUPS_DEEP
 #define PA_MMA_INT8_GROUPS_DEEP 2
 #endif
+
+// Grids of at least two blocks per resident slot run the persistent form (one CTA per
+// slot claiming items of a largest-first work list, the next item's copies overlapping
+// the current item).  Measured on GB300 it pays where the consumers' arithmetic, not
+// the copies, bounds the kernel and the batch is ragged: the int8 full-context
+// producer (bs64 ragged: 180.8 -> 174.5 us alone, step 181.7 -> 177.8 us).  bf16 and
+// sliding-window steps ran 2-4% slower with it (their blocks' starts already hide
+// behind the other resident blocks), so they keep one block per item.
+#ifndef PA_MMA_BF16_PERSIST
+#define PA_MMA_BF16_PERSIST 0
+#endif
+#ifndef PA_MMA_INT8_PERSIST
+#define PA_MMA_INT8_PERSIST 1
+#endif
+#ifndef PA_MMA_WINDOW_PERSIST
+#define PA_MMA_WINDOW_PERSIST 0
+#endif

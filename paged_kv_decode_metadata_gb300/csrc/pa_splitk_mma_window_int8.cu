@@ -10,7 +10,7 @@ cudaError_t launch_splitk_mma_window_int8(const SplitKParams& p, int bs, int gro
   return mma::launch_mma_impl<true, PA_MMA_INT8_STAGES1, PA_MMA_INT8_MINB1, PA_MMA_INT8_STAGES2,
                               PA_MMA_INT8_MINB2,
                               PA_MMA_SMALL_GRID_DEEP ? PA_MMA_INT8_STAGES_DEEP : 0, true,
-                              PA_MMA_INT8_GROUPS_DEEP>(
+                              PA_MMA_INT8_GROUPS_DEEP, PA_MMA_WINDOW_PERSIST>(
       p, bs, group, page_size, stream, use_pdl);
 }
 

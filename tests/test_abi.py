@@ -217,7 +217,7 @@ def test_instrumented_build_exports_its_header_and_production_does_not():
     ts = B.load_instrumented()
     text = re.sub(r"/\*.*?\*/", "", open(TS_HEADER).read(), flags=re.S)
     names = sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
-    assert names == ["pa_set_test_hold_loads", "pa_set_timestamp_buffer"]
+    assert names == ["pa_set_test_hold_loads", "pa_set_test_no_persist", "pa_set_timestamp_buffer"]
     for n in names + declared_functions():
         assert hasattr(ts, n), n
     prod = ctypes.CDLL(build.LIB_PATH)
