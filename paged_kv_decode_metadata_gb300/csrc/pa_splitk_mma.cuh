@@ -258,13 +258,26 @@ __device__ __forceinline__ void load_q_fragments(const SplitKParams& prm, int q_
     const __nv_bfloat16* qr = static_cast<const __nv_bfloat16*>(prm.q) +
                               (static_cast<int64_t>(q_begin + qi) * prm.num_q_heads + head) * 128;
     if constexpr (kF16) {
+      // a lane's 32 channels are 64 contiguous bytes of the row (rows are 256 bytes and
+      // Q is 16-byte aligned): four 16-byte loads
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 r = live ? reinterpret_cast<const uint4*>(qr + 32 * tig)[k]
+                             : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * k] = r.x;
+        w[4 * k + 1] = r.y;
+        w[4 * k + 2] = r.z;
+        w[4 * k + 3] = r.w;
+      }
       float v[8][4];
       float amax = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          v[j][u] = live ? __bfloat162float(qr[32 * tig + 4 * j + u]) : 0.f;
+          const uint32_t pair = w[2 * j + (u >> 1)];  // channels 4j + u, low half first
+          v[j][u] = __uint_as_float((u & 1) ? (pair & 0xffff0000u) : (pair << 16));
           amax = fmaxf(amax, fabsf(v[j][u]));
         }
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
@@ -319,8 +332,9 @@ __device__ __forceinline__ int64_t column_slot(int q_begin, int col, int G, int 
 // kPersist: the persistent form.  The grid is one CTA per resident slot; each CTA walks
 // a list of (request, kv head, split) items, built in shared memory from the request
 // lengths: the splits with a full page range first (all the same size), then the
-// partial last splits of each request, largest first, handed out in snake order over
-// the CTAs so that the slots finish together.  The ring keeps cycling across items, so
+// partial last splits of each request, largest first; a CTA claims the next item from
+// an atomic counter whenever its TMA warp is free to issue one, so the slots finish
+// together however the lengths are spread.  The ring keeps cycling across items, so
 // the TMA warp copies the next item's first chunks while the consumers finish the
 // current one (a fresh block would wait ~2 us for its first data).  One consumer group,
 // one query per request, at most kMaxPersistRequests requests.
@@ -334,9 +348,12 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
   constexpr int kConsumerWarps = NG * kGroupWarps;
   constexpr int kThreads = threads_of<NG>();
   using L = Layout<kQuant, STAGES, kConsumerWarps>;
-  // output merge buffer: [consumer warps][8 * kNT columns][128 channels] fp32; the
-  // persistent form merges in the stage of the item's last chunk (held until then)
-  constexpr int kRedBytes = kConsumerWarps * 8 * kNT * 128 * 4;
+  // output merge buffer: [consumer warps][8 * kNT columns][kRedStride] fp32 (128
+  // channels; the 4-float pad puts the columns a warp stores at once in different
+  // banks); the persistent form merges in the stage of the item's last chunk (held
+  // until then)
+  constexpr int kRedStride = 132;
+  constexpr int kRedBytes = kConsumerWarps * 8 * kNT * kRedStride * 4;
   static_assert(kRedBytes <= STAGES * L::STAGE_BYTES, "merge buffer reuses the ring");
   static_assert(!kPersist || kRedBytes <= L::STAGE_BYTES, "merge buffer fits one stage");
   constexpr bool kF16 = kQuant;
@@ -750,10 +767,12 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
   // m_run: the reference maximum the weights are relative to (warp-uniform per column);
   // t_max: this thread's true maximum of its own scores, reduced once per split.
   // ref: m_run, or 0 while a column has no score yet (its scores are all -inf then)
-  float m_run[kNT][2], l_part[kNT][2], t_max[kNT][2], ref[kNT][2];
+  // thr: m_run + kMaxSlack, the score above which the reference moves
+  float m_run[kNT][2], l_part[kNT][2], t_max[kNT][2], ref[kNT][2], thr[kNT][2];
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) {
     m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
+    thr[nt][0] = thr[nt][1] = -CUDART_INF_F;
     t_max[nt][0] = t_max[nt][1] = -CUDART_INF_F;
     l_part[nt][0] = l_part[nt][1] = 0.f;
     ref[nt][0] = ref[nt][1] = 0.f;
@@ -818,12 +837,18 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
       }
 
       // ---- S^T = K Q^T for tokens t0..t0+15 (M = 16 tokens, N = 8 heads per n-tile) --
-      // two accumulators (even / odd k-steps) halve the dependent MMA chain
+      // two accumulators (even / odd k-steps) halve the dependent MMA chain; int8 with
+      // one n-tile: the odd one starts at -kbias, which takes the +1152 of the K codes
+      // back out (two n-tiles subtract it afterwards, which keeps the register count down)
+      constexpr bool kBiasInAcc = kQuant && kNT == 1;
       float acc[2][kNT][4];
 #pragma unroll
-      for (int a = 0; a < 2; ++a)
+      for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) acc[a][nt][0] = acc[a][nt][1] = acc[a][nt][2] = acc[a][nt][3] = 0.f;
+        for (int i = 0; i < 4; ++i) {
+          acc[0][nt][i] = 0.f;
+          acc[1][nt][i] = kBiasInAcc ? -kbias[nt][i & 1] : 0.f;
+        }
       if constexpr (!kQuant) {
         const int mi = lane >> 3;
         const int row = t0 + (lane & 7) + 8 * (mi & 1);
@@ -848,7 +873,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
           const uint32_t x0 = w0[j] ^ 0x80808080u, x1 = w1[j] ^ 0x80808080u;
           uint32_t a[4];
           // 1024 + (code + 128) = code + 1152, exact in fp16; the +1152 is removed
-          // from the score through kbias
+          // from the score through kbias (the odd accumulator's start)
           a[0] = __byte_perm(x0, 0x64646464u, 0x4140);  // token gid,     channels +0, +1
           a[1] = __byte_perm(x1, 0x64646464u, 0x4140);  // token gid + 8
           a[2] = __byte_perm(x0, 0x64646464u, 0x4342);  // token gid,     channels +2, +3
@@ -903,7 +928,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float v = (acc[0][nt][i] + acc[1][nt][i]);
-          if constexpr (kQuant) v -= kbias[nt][i & 1];
+          if constexpr (kQuant && !kBiasInAcc) v -= kbias[nt][i & 1];
           v *= qf[nt][i & 1];
           if constexpr (kQuant) v *= (i < 2 ? ks_a : ks_b);
           x[i] = v;
@@ -924,7 +949,9 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
         t_max[nt][0] = fmaxf(t_max[nt][0], mx0);
         t_max[nt][1] = fmaxf(t_max[nt][1], mx1);
         float alpha[2] = {1.f, 1.f}, p[4];
-        const bool grow = mx0 > m_run[nt][0] + kMaxSlack || mx1 > m_run[nt][1] + kMaxSlack;
+        // (two n-tiles: recomputed, which keeps the register count down)
+        const bool grow = kNT == 1 ? mx0 > thr[nt][0] || mx1 > thr[nt][1]
+                                   : mx0 > m_run[nt][0] + kMaxSlack || mx1 > m_run[nt][1] + kMaxSlack;
         if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
           for (int m = 4; m <= 16; m <<= 1) {
@@ -938,6 +965,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
               alpha[e] = fast_exp2(m_run[nt][e] - m_new);
               m_run[nt][e] = m_new;
               ref[nt][e] = m_new;
+              thr[nt][e] = m_new + kMaxSlack;
             }
           }
           if (alpha[0] != 1.f || alpha[1] != 1.f) {
@@ -1120,7 +1148,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     }
     return;
   }
-  // [warps][8 * kNT columns][128 channels]: the ring (its start, or the held stage)
+  // [warps][8 * kNT columns][kRedStride]: the ring (its start, or the held stage)
   const int held_stage = (gc + n_chunks - 1) % STAGES;
   float* red = reinterpret_cast<float*>(kPersist ? smem + held_stage * L::STAGE_BYTES : smem);
 #pragma unroll
@@ -1134,18 +1162,20 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
         for (int w = 0; w < kConsumerWarps; ++w) mrow = fmaxf(mrow, ml_s[(w * 16 + head) * 3 + 2]);
         float scale = m_run[nt][e] == -CUDART_INF_F ? 0.f : exp2f(m_run[nt][e] - mrow);
         if constexpr (kQuant) scale /= vmul;  // vmul: a power of two
-        float* dst = red + (warp * 8 * kNT + head) * 128;
+        float* dst = red + (warp * 8 * kNT + head) * kRedStride;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int ch0 = kQuant ? 16 * i + 2 * gid : 16 * i + gid;
-          const int ch1 = kQuant ? 16 * i + 2 * gid + 1 : 16 * i + gid + 8;
           float v0 = o[nt][i][e], v1 = o[nt][i][2 + e];
           if constexpr (kVBias) {
             v0 -= 1152.f * wsum[nt][e];
             v1 -= 1152.f * wsum[nt][2 + e];
           }
-          dst[ch0] = v0 * scale;
-          dst[ch1] = v1 * scale;
+          if constexpr (kQuant) {  // channels 16i + 2gid and the next one: one 8-byte store
+            *reinterpret_cast<float2*>(dst + 16 * i + 2 * gid) = make_float2(v0 * scale, v1 * scale);
+          } else {  // channels 16i + gid and 16i + gid + 8
+            dst[16 * i + gid] = v0 * scale;
+            dst[16 * i + gid + 8] = v1 * scale;
+          }
         }
       }
     }
@@ -1155,7 +1185,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float4 v = *reinterpret_cast<const float4*>(red + (w * 8 * kNT + head) * 128 + d);
+      const float4 v = *reinterpret_cast<const float4*>(red + (w * 8 * kNT + head) * kRedStride + d);
       sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
     }
     *reinterpret_cast<float4*>(
