@@ -110,6 +110,11 @@ typedef enum {
  *                    mapping is NULL
  *   page_size >= 1, max_seq_pages >= 0, (max_seq_pages-1)*page_size <
  *   req_to_token_stride when max_seq_pages > 0.
+ * With use_pdl, the inputs (req_pool_indices, seq_lens, the req_to_token entries and
+ * their full_to_swa_mapping entries) are read before the kernel waits on the previous
+ * grid, and the outputs are written after it: the kernel launched just before must
+ * not write those inputs after it triggers its dependents (a kernel that never
+ * triggers early, as any kernel written without PDL, is always fine).
  * Errors: PA_ERR_INVALID as listed in the file comment.
  */
 PA_API pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_t* seq_lens,
@@ -135,6 +140,8 @@ PA_API pa_status pa_build_metadata(const int64_t* req_pool_indices, const int64_
  *                           otherwise            -> 0
  *   num_out_tokens = min(swa_out_len, out_cache_loc_len)
  * swa_out_cache_loc [swa_out_len] int64 (out) or NULL; it needs the mapping.
+ * With use_pdl, qlens and out_cache_loc are inputs read before the wait too (the
+ * same rule as pa_build_metadata's inputs).
  */
 PA_API pa_status pa_build_metadata_full(
     const void* req_pool_indices, const void* seq_lens, int32_t index_bits,
@@ -279,7 +286,11 @@ PA_API pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const
  * pa_decode_step -- metadata, producer and reducer in one call (three launches; the
  * second and third carry the PDL attribute when use_pdl is non-zero, the first
  * too, and it waits before writing anything).  Arguments are those of the three
- * functions above.  The split-K scratch is carved from `workspace`
+ * functions above.  With use_pdl the step's inputs -- q and the metadata inputs --
+ * are read before the step waits on the kernel launched before it (the metadata
+ * kernel triggers its dependents on entry, so the producer's Q prologue can run while
+ * that kernel finishes): that kernel must not write them after it triggers its
+ * dependents (a kernel that never triggers early is always fine).  The split-K scratch is carved from `workspace`
  * (workspace_bytes >= pa_workspace_bytes(bs, num_q_heads, head_dim, S)), where S is
  * num_splits, or pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, kv_dtype, 0)
  * when num_splits == 0.
