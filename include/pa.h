@@ -290,10 +290,10 @@ PA_API pa_status pa_reduce(const float* scratch_m, const float* scratch_l, const
  * are read before the step waits on the kernel launched before it (the metadata
  * kernel triggers its dependents on entry, so the producer's Q prologue can run while
  * that kernel finishes): that kernel must not write them after it triggers its
- * dependents (a kernel that never triggers early is always fine).  The split-K scratch is carved from `workspace`
- * (workspace_bytes >= pa_workspace_bytes(bs, num_q_heads, head_dim, S)), where S is
- * num_splits, or pa_choose_splits(bs, num_kv_heads, max_seq_pages, page_size, kv_dtype, 0)
- * when num_splits == 0.
+ * dependents (a kernel that never triggers early is always fine).  The split-K
+ * scratch is carved from `workspace` (workspace_bytes >= pa_workspace_bytes(bs,
+ * num_q_heads, head_dim, S)), where S is num_splits, or pa_choose_splits(bs,
+ * num_kv_heads, max_seq_pages, page_size, kv_dtype, 0) when num_splits == 0.
  */
 PA_API pa_status pa_decode_step(
     const int64_t* req_pool_indices, const int64_t* seq_lens, const int32_t* req_to_token,
@@ -469,8 +469,7 @@ PA_API size_t pa_workspace_bytes(int32_t bs, int32_t num_q_heads, int32_t head_d
 
 /*
  * Split count heuristic, measured on GB300: a split holds about 2048 positions of the
- * longest request for bf16 KV and 4096 for int8 KV (whose producer spends more time
- * per block outside the KV stream), but there are at least 2.5 waves of
+ * longest request (bf16 and int8 KV alike), but there are at least 2.5 waves of
  * (request, kv head, split) blocks at three resident blocks per SM; each split holds at
  * least two 64-token chunks, its length is page-aligned, and no split count leaves the
  * longest request with an empty split.  kv_dtype is PA_KV_BF16 or PA_KV_INT8 (any other

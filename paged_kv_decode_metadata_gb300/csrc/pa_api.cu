@@ -422,11 +422,14 @@ int32_t pa_choose_splits(int32_t bs, int32_t num_kv_heads, int32_t max_seq_pages
   if (bs <= 0 || num_kv_heads <= 0 || max_seq_pages <= 0 || page_size <= 0) return 1;
   if (sm_count <= 0) sm_count = sm_count_of_current_device();
   if (sm_count <= 0) sm_count = 152;
-  // Positions of the longest request per split: the int8 producer's per-block work
-  // outside the KV stream (Q conversion, merge) favours longer splits (GB300 sweeps:
-  // best near 2048 for bf16, 4096 for int8, on uniform and ragged batches).
+  // About 2048 positions of the longest request per split, for both KV types (GB300
+  // sweeps of the whole step: bf16 bs32 ctx 8K best at 5 splits; int8 bs64 ctx 8K
+  // best at 4, ragged bs64 / bs32 up to 16K at 6-8, ragged bs64 up to 32K at 6-8 with
+  // 16 within 1.2%; the persistent form balances the smaller items that gives).
+  // kv_dtype is kept in the signature: the two types have differed.
+  (void)kv_dtype;
   const int64_t tokens = static_cast<int64_t>(max_seq_pages) * page_size;
-  int64_t want = cdiv(tokens, kv_dtype == PA_KV_INT8 ? 4096 : 2048);
+  int64_t want = cdiv(tokens, 2048);
   // ... but at least 2.5 waves of blocks at three resident blocks per SM, so the
   // scheduler can balance ragged requests and the last wave is not most of the step.
   const int64_t units = static_cast<int64_t>(bs) * num_kv_heads;

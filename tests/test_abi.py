@@ -201,9 +201,11 @@ def test_workspace_and_split_heuristic(lib):
             assert 1 <= s <= max(1, pages)
             pps = -(-pages // s)
             assert -(-pages // pps) == s          # the longest request has no empty split
-    # the GB300 sweep's best counts: bs32 ctx8K bf16, bs64 ctx16K int8, bs64 window 4096 int8
+    # the GB300 sweeps' best counts: bs32 ctx8K bf16, bs64 ctx8K int8, bs64 ctx16K int8
+    # (6 and 8 equal), bs64 window 4096 int8
     assert B.pa_choose_splits(32, 8, 128, 64, B.PA_KV_BF16, 152) == 5
-    assert B.pa_choose_splits(64, 8, 256, 64, B.PA_KV_INT8, 152) == 4
+    assert B.pa_choose_splits(64, 8, 128, 64, B.PA_KV_INT8, 152) == 4
+    assert B.pa_choose_splits(64, 8, 256, 64, B.PA_KV_INT8, 152) == 8
     assert B.pa_choose_splits(64, 8, 65, 64, B.PA_KV_INT8, 152) == 3
     assert B.pa_choose_splits(0, 8, 16, 64, B.PA_KV_BF16, 152) == 1
     assert B.pa_status_string(B.PA_ERR_UNSUPPORTED) == "unsupported shape"

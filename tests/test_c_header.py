@@ -20,7 +20,7 @@ int main(void) {
   size_t ws = pa_workspace_bytes(32, 32, 128, 5);
   if (ws != 2 * (size_t)(32 * 32 * 5 * 4) + (size_t)32 * 32 * 5 * 128 * 4) return 1;
   if (pa_choose_splits(32, 8, 128, 64, PA_KV_BF16, 152) != 5) return 2;
-  if (pa_choose_splits(64, 8, 256, 64, PA_KV_INT8, 152) != 4) return 3;
+  if (pa_choose_splits(64, 8, 256, 64, PA_KV_INT8, 152) != 8) return 3;
   if (pa_window_pages(4096, 1, 64, 256) != 65) return 4;
   if (strcmp(pa_status_string(PA_ERR_UNSUPPORTED), "unsupported shape") != 0) return 5;
   /* host validation returns before any launch */
