@@ -36,8 +36,10 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
-    ap.add_argument("--warmup", type=int, default=50)
+    # defaults: 5000 / 50 GPU steps; the reference arm (whole oracle steps of ~0.1 s on
+    # 16 host cores) defaults to 20 / 3 so that a run without flags ends in seconds
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="bs32_ctx8k")
     ap.add_argument("--no-extras", action="store_true",
@@ -51,7 +53,13 @@ def parse():
     ap.add_argument("--all-workloads", action="store_true",
                     help="report table: every named workload, graph with / without PDL and "
                          "eager (one JSON line per workload; not the benchmark line)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    ref = args.impl == "reference"
+    if args.steps is None:
+        args.steps = 20 if ref else 5000
+    if args.warmup is None:
+        args.warmup = 3 if ref else 50
+    return args
 
 
 def measured_peaks():
