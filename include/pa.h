@@ -10,7 +10,13 @@
  * request) and pa_decode_splitk_window / pa_decode_step_window (sliding-window layers)
  * are the producer's other forms.  Every entry point takes plain device pointers
  * and sizes, enqueues work on `stream` (a cudaStream_t passed as void*, NULL = the
- * legacy default stream) and returns without synchronising.  No entry point
+ * legacy default stream) and returns without synchronising.  The step's own inputs
+ * and outputs -- q, req_pool_indices, seq_lens, out, lse -- may instead point into
+ * pinned host memory (cudaHostAlloc / cudaHostRegister; with unified addressing the
+ * host pointer is the device pointer): the kernels then read and write them over the
+ * host link, with no copy on the stream; the result is the same bit for bit.  The
+ * K/V pools, scales, req_to_token, metadata outputs and scratch stay in device
+ * memory.  No entry point
  * allocates memory: the caller owns every buffer, including the split-K scratch
  * (pa_decode_step_static_scratch uses a scratch array inside the library instead).
  * The metadata, producer, reducer and pa_decode_step(_window) launches are recorded

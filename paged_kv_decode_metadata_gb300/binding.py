@@ -168,6 +168,21 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
     return t.data_ptr()
 
 
+def _io_ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    """Pointer of a step input or output that the kernels may also reach in pinned host
+    memory (q, req_pool_indices, seq_lens, out, lse): a CUDA tensor, or a pinned CPU
+    tensor, which the kernels then read or write over the host link (no copy)."""
+    if t is not None and not t.is_cuda:
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+        if dtype is not None and t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        return t.data_ptr()
+    return _ptr(t, dtype, name)
+
+
 def _row_stride(t: torch.Tensor, name: str) -> int:
     if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
         raise ValueError(f"{name} must be 2-D with unit column stride")
@@ -218,8 +233,8 @@ def pa_build_metadata_full(req_pool_indices, seq_lens, req_to_token, cache_seqle
     if idx_dtype not in (torch.int64, torch.int32):
         raise ValueError("req_pool_indices must be int64 or int32")
     st = lib.pa_build_metadata_full(
-        _ptr(req_pool_indices, idx_dtype, "req_pool_indices"),
-        _ptr(seq_lens, idx_dtype, "seq_lens"), 64 if idx_dtype == torch.int64 else 32,
+        _io_ptr(req_pool_indices, idx_dtype, "req_pool_indices"),
+        _io_ptr(seq_lens, idx_dtype, "seq_lens"), 64 if idx_dtype == torch.int64 else 32,
         _ptr2d(req_to_token, torch.int32, "req_to_token"),
         req_to_token.shape[0], req_to_token.stride(0),
         _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
@@ -259,7 +274,7 @@ def pa_decode_splitk(q, k_cache, v_cache, page_table, cache_seqlens, scratch_m, 
     bs, hq, d = q.shape
     num_pages, hkv, page_size, _ = k_cache.shape
     st = lib.pa_decode_splitk(
-        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
+        _io_ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
         ks, vs, kv_dtype, _ptr2d(page_table, torch.int32, "page_table"),
         _row_stride(page_table, "page_table"),
         _ptr(cache_seqlens, torch.int32, "cache_seqlens"), bs, hq, hkv, d, page_size, num_pages,
@@ -281,7 +296,7 @@ def pa_decode_splitk_multi(q, k_cache, v_cache, page_table, cache_seqlens, cu_se
     bs = cache_seqlens.shape[0]
     num_pages, hkv, page_size, _ = k_cache.shape
     st = lib.pa_decode_splitk_multi(
-        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
+        _io_ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
         ks, vs, kv_dtype, _ptr2d(page_table, torch.int32, "page_table"),
         _row_stride(page_table, "page_table"), _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
         _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q"), bs, int(max_q_len), hq, hkv, d,
@@ -305,7 +320,7 @@ def pa_decode_splitk_window(q, k_cache, v_cache, page_table, cache_seqlens, scra
     bs = cache_seqlens.shape[0]
     num_pages, hkv, page_size, _ = k_cache.shape
     st = lib.pa_decode_splitk_window(
-        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
+        _io_ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"),
         ks, vs, kv_dtype, _ptr2d(page_table, torch.int32, "page_table"),
         _row_stride(page_table, "page_table"), _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
         _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q"), bs, int(max_q_len), hq, hkv, d,
@@ -332,7 +347,7 @@ def pa_reduce(scratch_m, scratch_l, scratch_acc, out, lse=None, *, stream=None,
     st = lib.pa_reduce(_ptr(scratch_m, torch.float32, "scratch_m"),
                        _ptr(scratch_l, torch.float32, "scratch_l"),
                        _ptr(scratch_acc, torch.float32, "scratch_acc"), bs, hq, d, s,
-                       _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+                       _io_ptr(out, torch.bfloat16, "out"), _io_ptr(lse, torch.float32, "lse"),
                        _stream(stream), int(bool(use_pdl)))
     _check("pa_reduce", st)
 
@@ -354,8 +369,8 @@ def _decode_step_args(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset
     bs, hq, d = q.shape
     num_pages, hkv, page_size, _ = k_cache.shape
     return (
-        _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
-        _ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
+        _io_ptr(req_pool_indices, torch.int64, "req_pool_indices"),
+        _io_ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
         req_to_token.shape[0], req_to_token.stride(0),
         _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
         full_to_swa_mapping.numel() if full_to_swa_mapping is not None else 0,
@@ -364,11 +379,11 @@ def _decode_step_args(*, req_pool_indices, seq_lens, req_to_token, seqlen_offset
         _row_stride(page_table, "page_table"),
         _ptr2d(swa_page_table, torch.int32, "swa_page_table") if swa_page_table is not None else None,
         _row_stride(swa_page_table, "swa_page_table") if swa_page_table is not None else 0,
-        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"),
+        _io_ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"),
         _ptr(v_cache, None, "v_cache"), ks, vs, kv_dtype, bs, hq, hkv, d, page_size, num_pages,
         int(num_splits), float(sm_scale), _ptr(workspace, None, "workspace"),
-        workspace.numel() * workspace.element_size(), _ptr(out, torch.bfloat16, "out"),
-        _ptr(lse, torch.float32, "lse"), _stream(stream), int(bool(use_pdl)))
+        workspace.numel() * workspace.element_size(), _io_ptr(out, torch.bfloat16, "out"),
+        _io_ptr(lse, torch.float32, "lse"), _stream(stream), int(bool(use_pdl)))
 
 
 def _host_ptr(t, dtype, name):
@@ -437,8 +452,8 @@ def pa_decode_step_multi(*, req_pool_indices, seq_lens, req_to_token, seqlen_off
     bs = cache_seqlens.shape[0]
     num_pages, hkv, page_size, _ = k_cache.shape
     st = lib.pa_decode_step_multi(
-        _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
-        _ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
+        _io_ptr(req_pool_indices, torch.int64, "req_pool_indices"),
+        _io_ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
         req_to_token.shape[0], req_to_token.stride(0),
         _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
         full_to_swa_mapping.numel() if full_to_swa_mapping is not None else 0,
@@ -448,11 +463,11 @@ def pa_decode_step_multi(*, req_pool_indices, seq_lens, req_to_token, seqlen_off
         _ptr2d(swa_page_table, torch.int32, "swa_page_table") if swa_page_table is not None else None,
         _row_stride(swa_page_table, "swa_page_table") if swa_page_table is not None else 0,
         _ptr(qlens, torch.int64, "qlens"), int(q_mode), int(q_stride),
-        _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _ptr(q, torch.bfloat16, "q"), total_q,
+        _ptr(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _io_ptr(q, torch.bfloat16, "q"), total_q,
         int(max_q_len), _ptr(k_cache, None, "k_cache"), _ptr(v_cache, None, "v_cache"), ks, vs,
         kv_dtype, bs, hq, hkv, d, page_size, num_pages, int(num_splits), float(sm_scale),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
-        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream),
+        _io_ptr(out, torch.bfloat16, "out"), _io_ptr(lse, torch.float32, "lse"), _stream(stream),
         int(bool(use_pdl)))
     _check("pa_decode_step_multi", st)
 
@@ -475,19 +490,19 @@ def _decode_step_window_args(*, req_pool_indices, seq_lens, req_to_token, seqlen
     bs, hq, d = q.shape
     num_pages, hkv, page_size, _ = k_swa.shape
     return (
-        _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
-        _ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
+        _io_ptr(req_pool_indices, torch.int64, "req_pool_indices"),
+        _io_ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
         req_to_token.shape[0], req_to_token.stride(0),
         _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
         full_to_swa_mapping.numel(), int(seqlen_offset), int(max_seq_pages),
         _ptr(cache_seqlens, torch.int32, "cache_seqlens"),
         _ptr(cu_seqlens_k, torch.int32, "cu_seqlens_k"), _ptr2d(page_table, torch.int32, "page_table"),
         _row_stride(page_table, "page_table"), _ptr2d(swa_page_table, torch.int32, "swa_page_table"),
-        _row_stride(swa_page_table, "swa_page_table"), _ptr(q, torch.bfloat16, "q"),
+        _row_stride(swa_page_table, "swa_page_table"), _io_ptr(q, torch.bfloat16, "q"),
         _ptr(k_swa, None, "k_swa"), _ptr(v_swa, None, "v_swa"), ks, vs, kv_dtype, bs, hq, hkv, d,
         page_size, num_pages, int(sliding_window), int(num_splits), float(sm_scale),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
-        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream),
+        _io_ptr(out, torch.bfloat16, "out"), _io_ptr(lse, torch.float32, "lse"), _stream(stream),
         int(bool(use_pdl)))
 
 
@@ -543,8 +558,8 @@ def pa_decode_step_static_scratch(*, req_pool_indices, seq_lens, req_to_token,
     bs, hq, d = q.shape
     num_pages, hkv, page_size, _ = k_cache.shape
     st = lib.pa_decode_step_static_scratch(
-        _ptr(req_pool_indices, torch.int64, "req_pool_indices"),
-        _ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
+        _io_ptr(req_pool_indices, torch.int64, "req_pool_indices"),
+        _io_ptr(seq_lens, torch.int64, "seq_lens"), _ptr2d(req_to_token, torch.int32, "req_to_token"),
         req_to_token.shape[0], req_to_token.stride(0),
         _ptr(full_to_swa_mapping, torch.int64, "full_to_swa_mapping"),
         full_to_swa_mapping.numel() if full_to_swa_mapping is not None else 0,
@@ -553,10 +568,10 @@ def pa_decode_step_static_scratch(*, req_pool_indices, seq_lens, req_to_token,
         _row_stride(page_table, "page_table"),
         _ptr2d(swa_page_table, torch.int32, "swa_page_table") if swa_page_table is not None else None,
         _row_stride(swa_page_table, "swa_page_table") if swa_page_table is not None else 0,
-        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"),
+        _io_ptr(q, torch.bfloat16, "q"), _ptr(k_cache, None, "k_cache"),
         _ptr(v_cache, None, "v_cache"), ks, vs, kv_dtype, bs, hq, hkv, d, page_size, num_pages,
-        int(num_splits), float(sm_scale), _ptr(out, torch.bfloat16, "out"),
-        _ptr(lse, torch.float32, "lse"), _stream(stream), int(bool(use_pdl)))
+        int(num_splits), float(sm_scale), _io_ptr(out, torch.bfloat16, "out"),
+        _io_ptr(lse, torch.float32, "lse"), _stream(stream), int(bool(use_pdl)))
     _check("pa_decode_step_static_scratch", st)
 
 

@@ -156,6 +156,17 @@ class DeviceStep:
             self._prepared[key] = call
         call()
 
+    def prepare_host_io_step(self, h_inputs, h_outputs, use_pdl=True, stream=None):
+        """A prepared step whose q, req_pool_indices and seq_lens (in ``h_inputs``) and
+        out and lse (in ``h_outputs``) live in pinned host memory with the layout of
+        ``host_buffers()``: the kernels read and write them over the host link, so the
+        stream holds the three kernels and no copy."""
+        q, rpi, sl = self._input_views(h_inputs)
+        out, lse = self._output_views(h_outputs)
+        kw = self._step_kwargs()
+        kw.update(q=q, req_pool_indices=rpi, seq_lens=sl, out=out, lse=lse)
+        return self._prepare(stream=B._stream(stream), use_pdl=use_pdl, **kw)
+
     def prepare_host_step(self, h_q, h_req_pool_indices, h_seq_lens, h_out, h_lse=None,
                           use_pdl=True, stream=None):
         """A prepared ``pa_decode_step_host`` call: host inputs copied into this step's

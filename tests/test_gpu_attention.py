@@ -299,6 +299,71 @@ def test_host_buffer_step_matches_device_step(packed):
     _check_flags()
 
 
+def test_host_packed_step_in_cuda_graph():
+    """pa_decode_step_host_packed captured once into a CUDA graph: every replay copies
+    the host inputs as they are at that replay and writes the host outputs, bit for bit
+    pa_decode_step's on the same inputs."""
+    wl, ds = named("bs8_ctx1k")
+    h_in, h_outs, (h_q, h_rpi, h_sl, h_out, h_lse) = ds.host_buffers()
+    h_rpi.copy_(wl.req_pool_indices)
+    h_sl.copy_(wl.seq_lens)
+    stream = torch.cuda.Stream()
+    call = ds.prepare_packed_host_step(h_in, h_outs, use_pdl=True, stream=stream)
+    h_q.copy_(wl.q)
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    torch.cuda.synchronize()
+    for rep in range(2):
+        q = synthetic.draw_queries(wl.spec.bs, wl.spec.num_q_heads, wl.spec.head_dim, 90 + rep)
+        h_q.copy_(q)
+        h_out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(ds.q.cpu(), q)
+        ds.step()
+        torch.cuda.synchronize()
+        assert torch.equal(h_out, ds.out.cpu()) and torch.equal(h_lse, ds.lse.cpu())
+    del graph
+    ds.q.copy_(wl.q)
+    _check_flags()
+
+
+@pytest.mark.parametrize("name", ["bs8_ctx1k", "bs64_ragged16k_int8_swa"])
+def test_host_io_step_matches_device_step(name):
+    """pa_decode_step with q, req_pool_indices, seq_lens, out and lse in pinned host
+    memory (the kernels read and write them over the host link; no copies), eager and
+    from a CUDA graph: bit for bit pa_decode_step's on device buffers."""
+    wl, ds = named(name)
+    ds.step()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = ds.out.cpu(), ds.lse.cpu()
+    h_in, h_outs, (h_q, h_rpi, h_sl, h_out, h_lse) = ds.host_buffers()
+    h_q.copy_(ds.q)
+    h_rpi.copy_(ds.req_pool_indices)
+    h_sl.copy_(ds.seq_lens)
+    stream = torch.cuda.Stream()
+    call = ds.prepare_host_io_step(h_in, h_outs, use_pdl=True, stream=stream)
+    call()
+    stream.synchronize()
+    assert torch.equal(h_out, ref_out) and torch.equal(h_lse, ref_lse)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    torch.cuda.synchronize()
+    h_out.zero_()
+    h_lse.zero_()
+    with torch.cuda.stream(stream):
+        graph.replay()
+    stream.synchronize()
+    assert torch.equal(h_out, ref_out) and torch.equal(h_lse, ref_lse)
+    del graph
+    _check_flags()
+
+
 def test_page_relabelling_bit_identical_on_gpu():
     spec = synthetic.Spec("relabel", bs=4, num_q_heads=32, num_kv_heads=8, num_pages=80,
                           ragged=(300, 1200), num_splits=5, seed=902)
