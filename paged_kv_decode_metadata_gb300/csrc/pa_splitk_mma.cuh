@@ -12,9 +12,10 @@
 // (G = 4 bf16).  One m16n8k16 MMA does 2048 multiply-adds per warp instruction.
 //
 // GB300 mapping
-//   * CTA = 4 consumer warps (4 * NG for small grids) + 1 producer warp.  The producer warp's lane 0 streams
-//     64-token chunks with 4-D TMA tiled copies (cp.async.bulk.tensor) of the
-//     [num_pages, Hkv, page_size, 128] pools into a STAGES-deep ring; full/empty
+//   * CTA = 4 consumer warps (4 * NG for small grids) + 1 producer warp.  The producer
+//     warp's lane 0 streams 64-token chunks with 4-D TMA tiled copies
+//     (cp.async.bulk.tensor) of the [num_pages, Hkv, page_size, 128] pools into a
+//     STAGES-deep ring; full/empty
 //     mbarriers hand stages back and forth, so there is no CTA-wide barrier per chunk.
 //     128-byte swizzle makes every ldmatrix / 16-byte shared load conflict free.
 //     Grids of at most one block per SM take a deeper ring at one CTA per SM.
@@ -23,9 +24,13 @@
 //     tokens; the warps' states are merged once at the end of the split (the same
 //     log-sum-exp combination the reducer applies across splits).  One group consumes
 //     every chunk; grids of at most one block per SM use several groups, each taking
-//     every NG-th chunk, so a short split's chunks are worked on at once.  The weights of a column are relative to a reference maximum that moves
-//     only when a score passes it by more than 2^kMaxSlack (log2 units), so most slices
-//     need one warp vote instead of a shuffle reduction and a rescale.
+//     every NG-th chunk, so a short split's chunks are worked on at once.  The weights
+//     of a column are relative to a reference maximum that moves only when a score
+//     passes it by more than 2^kMaxSlack (log2 units), so most slices need one warp
+//     vote instead of a shuffle reduction and a rescale.
+//   * Persistent form (kPersist; large int8 grids): one CTA per resident slot claims
+//     (request, kv head, split) items from a largest-first work list, and the ring keeps
+//     cycling across items.
 //   * Transposed orientation: S^T = K Q^T with M = 16 tokens, N = 8 columns (a column is
 //     a query head, or a (query, head) pair with several queries per request), K = 16
 //     channels; then O^T += V^T P^T with M = 16 channels, K = 16 tokens, and P^T taken
@@ -37,10 +42,10 @@
 //     fp16 MMAs.  K: 16-byte shared loads, with the contraction order over channels
 //     permuted so that each lane reads 16 contiguous bytes (QK^T does not depend on
 //     that order).  V: ldmatrix.trans hands each lane two tokens of one channel, the
-//     pair an A register of V^T holds.  Both K and V codes enter biased by +1152: the
-//     resulting 1152 * sum(q) per column is subtracted from the fp32 score, and 1152
-//     times each column's sum of fp16 weights (accumulated by an all-ones MMA) from the
-//     output every kBiasPeriod chunks.  Q is scaled per column by a power of two into
+//     pair an A register of V^T holds.  Both K and V codes come out biased by +1152: the
+//     resulting 1152 * sum(q) per column is taken out of the fp32 score (the odd QK^T
+//     accumulator starts at its negative), and the V codes get the bias subtracted in
+//     fp16 (exact) before the PV product.  Q is scaled per column by a power of two into
 //     fp16's range (bf16 values stay exact; the factor returns in the fp32 score
 //     scale).  The K scale multiplies the fp32 score; the V scale folds into the fp16
 //     softmax weight, prescaled per warp by a power of two so that no significant
