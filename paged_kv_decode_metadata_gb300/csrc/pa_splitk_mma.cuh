@@ -517,6 +517,17 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
   // that holds its first chunk.
   unsigned int* claims = kPersist ? g_work_claims[prm.work_slot] : nullptr;
   int32_t* desc_s = reinterpret_cast<int32_t*>(smem + L::OFF_DESC);
+  // TMA warp lane 0, once per CTA: this CTA claims nothing more; the last CTA to get
+  // here sets the launch's counters back to zero for the slot's next launch (also when
+  // the CTA stops early, so a failed launch leaves its slot clean)
+  auto finish_claims = [&]() {
+    __threadfence();
+    if (atomicAdd(claims + 1, 1u) == gridDim.x - 1) {
+      claims[0] = 0;
+      claims[1] = 0;
+      __threadfence();
+    }
+  };
 
   // ring position: chunks this thread's role has issued (TMA warp) or consumed so far
   int gc = 0;
@@ -629,7 +640,10 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     // failure-detection test of the instrumented build: nothing is issued, so every
     // consumer wait gives up after its time limit and the kernel reports it
     if (prm.hold_loads) {
-      if (lane == 0) *producer_done = 1;
+      if (lane == 0) {
+        if constexpr (kPersist) finish_claims();
+        *producer_done = 1;
+      }
       trigger_dependents();
       return;
     }
@@ -1236,13 +1250,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
             mbar_arrive(&full[stage]);
           }
         }
-        // this CTA claims nothing more; the last CTA to get here resets the counter
-        __threadfence();
-        if (atomicAdd(claims + 1, 1u) == gridDim.x - 1) {
-          claims[0] = 0;
-          claims[1] = 0;
-          __threadfence();
-        }
+        finish_claims();
       }
       // stopped early: the consumers have given up, so nothing else waits for these
       if (*abort_flag) drain_issued(*issued_s);
