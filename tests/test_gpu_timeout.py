@@ -69,3 +69,54 @@ def test_wait_limit_reports_and_returns(ts):
         torch.cuda.synchronize()
         assert B.pa_read_error_flags(reset=True, lib=ts) == 0
     assert_attention_close(out, lse, oracle_attention(wl, meta), "after timeout")
+
+
+def test_persistent_form_recovers_after_timeout(ts):
+    """An int8 batch large enough for the persistent form (one CTA per resident slot
+    claiming items from a per-launch counter slot): with the hook on, every CTA's
+    consumers time out and the launch reports it; with the hook off, the next 70
+    launches (every counter slot reused at least once) each give the oracle's answer."""
+    spec = synthetic.Spec("stall8", bs=32, num_q_heads=64, num_kv_heads=8, num_pages=300,
+                          ctx=512, kv_dtype="int8", num_splits=4, seed=78)
+    wl = synthetic.make(spec)
+    meta = oracle_metadata(wl)
+    dev = "cuda"
+    f32 = dict(dtype=torch.float32, device=dev)
+    S = spec.num_splits
+    q, k, v = wl.q.to(dev), wl.k_cache.to(dev), wl.v_cache.to(dev)
+    ks, vs = wl.k_scale.to(dev), wl.v_scale.to(dev)
+    pt = torch.from_numpy(meta["page_table"]).to(dev)
+    cl = torch.from_numpy(meta["cache_seqlens"]).to(dev)
+    m = torch.empty((spec.bs, spec.num_q_heads, S), **f32)
+    l = torch.empty((spec.bs, spec.num_q_heads, S), **f32)
+    acc = torch.empty((spec.bs, spec.num_q_heads, S, 128), **f32)
+    out = torch.empty((spec.bs, spec.num_q_heads, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((spec.bs, spec.num_q_heads), **f32)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+
+    def splitk():
+        return ts.pa_decode_splitk(p(q), p(k), p(v), p(ks), p(vs), B.PA_KV_INT8, p(pt),
+                                   pt.stride(0), p(cl), spec.bs, spec.num_q_heads,
+                                   spec.num_kv_heads, 128, spec.page_size, spec.num_pages,
+                                   wl.max_seq_pages, S, wl.sm_scale, p(m), p(l), p(acc),
+                                   None, 0)
+
+    with B.producer(B.PA_PRODUCER_MMA):
+        assert ts.pa_set_test_hold_loads(1) == B.PA_OK
+        try:
+            assert splitk() == B.PA_OK
+            torch.cuda.synchronize()
+        finally:
+            ts.pa_set_test_hold_loads(0)
+        flags = B.pa_read_error_flags(reset=True, lib=ts)
+        assert flags & B.DEVERR_WAIT_TIMEOUT, hex(flags)
+        ref = oracle_attention(wl, meta)
+        for rep in range(70):
+            acc.fill_(float("nan"))
+            assert splitk() == B.PA_OK
+            if rep % 10 == 9 or rep == 0:
+                assert ts.pa_reduce(p(m), p(l), p(acc), spec.bs, spec.num_q_heads, 128, S,
+                                    p(out), p(lse), None, 0) == B.PA_OK
+                torch.cuda.synchronize()
+                assert B.pa_read_error_flags(reset=True, lib=ts) == 0
+                assert_attention_close(out, lse, ref, f"launch {rep} after timeout")
