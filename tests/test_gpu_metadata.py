@@ -173,3 +173,16 @@ def test_empty_batch_is_a_no_op():
                         torch.full((1,), 3, **i32), torch.empty((0, 1), **i32), seqlen_offset=0,
                         max_seq_pages=1, page_size=64)
     torch.cuda.synchronize()
+
+
+def test_metadata_long_rows_and_many_requests():
+    """Rows longer than the 1024 columns a row block reads before its PDL wait (the
+    rest is read after it) and more requests than one 256-wide scan tile (later tiles
+    of lengths are read after the wait): still bit-exact, sliding-window table too."""
+    spec = synthetic.Spec("long_rows", bs=300, num_q_heads=8, num_kv_heads=8,
+                          num_pages=400000, ragged=(1, 20000), page_size=16,
+                          swa_window=5000, seqlen_offset=1, seed=404)
+    wl = synthetic.make(spec, with_cache=False)
+    assert wl.max_seq_pages > 1024
+    for use_pdl in (True, False):
+        _compare(_run(wl, stride_pad=2, use_pdl=use_pdl), oracle_metadata(wl), wl.max_seq_pages)
