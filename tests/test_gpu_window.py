@@ -153,6 +153,16 @@ def test_window_step_bs64_ragged_int8():
     ref = Expected(paged_attention_window_threaded, bits(wl.q), k, v, meta["swa_page_table"],
                    meta["cache_seqlens"], wl.spec.swa_window, wl.sm_scale, ks, vs)
     assert_attention_close(ws.out, ws.lse, ref, "bs64 window")
+    # the same step with q / req_pool_indices / seq_lens / out / lse in pinned host
+    # memory (no copies): the same bits
+    h_in, h_outs, (h_q, h_rpi, h_sl, h_out, h_lse) = ws.host_buffers()
+    h_q.copy_(ws.q)
+    h_rpi.copy_(ws.req_pool_indices)
+    h_sl.copy_(ws.seq_lens)
+    ws.prepare_host_io_step(h_in, h_outs, use_pdl=True)()
+    torch.cuda.synchronize()
+    assert torch.equal(h_out, ws.out.cpu()) and torch.equal(h_lse, ws.lse.cpu())
+    assert B.pa_read_error_flags(reset=True) == 0
 
 
 def test_window_rejects_bad_arguments():
