@@ -85,3 +85,40 @@ def test_persistent_form_in_a_cuda_graph_of_steps(ts_lib):
         torch.cuda.synchronize()
         assert torch.equal(ds.out, want[0]) and torch.equal(ds.lse, want[1])
     assert B.pa_read_error_flags(reset=True) == 0
+
+
+def _persist_spec(seed):
+    """A random int8 full-context batch big enough for the persistent form: G in
+    {1, 2, 4, 8}, Hkv in {1, 2, 4, 8}, page 16-128, ragged lengths, 2-24 splits."""
+    g = torch.Generator().manual_seed(70_000 + seed)
+    pick = lambda xs: xs[int(torch.randint(0, len(xs), (1,), generator=g))]  # noqa: E731
+    grp, hkv, P = pick([1, 2, 4, 8]), pick([1, 2, 4, 8]), pick([16, 32, 64, 128])
+    ctx_max = pick([300, 2000, 9000])
+    slots = 3 * torch.cuda.get_device_properties(0).multi_processor_count
+    splits = int(torch.randint(2, 25, (1,), generator=g))
+    bs = max(int(torch.randint(1, 129, (1,), generator=g)), -(-2 * slots // (splits * hkv)))
+    bs = min(bs, 128)
+    return synthetic.Spec(f"persist_fuzz{seed}", bs=bs, num_q_heads=grp * hkv, num_kv_heads=hkv,
+                          num_pages=bs * (-(-ctx_max // P)) + 2, ragged=(1, ctx_max),
+                          page_size=P, kv_dtype="int8", num_splits=splits,
+                          seqlen_offset=int(torch.randint(0, 2, (1,), generator=g)),
+                          seed=71_000 + seed)
+
+
+# 8 seeds by default; PA_PERSIST_SEEDS=n draws n
+@pytest.mark.parametrize("seed", range(int(__import__("os").environ.get("PA_PERSIST_SEEDS", "8"))))
+def test_persistent_form_random_batches(ts_lib, seed):
+    """Random batches that take the persistent form (at least two blocks per resident
+    slot, at most 128 requests): the same bits as one block per item, every request
+    against the oracle."""
+    spec = _persist_spec(seed)
+    wl = synthetic.make(spec)
+    ds = DeviceStep(wl)
+    if ds.num_splits * spec.num_kv_heads * spec.bs < 2 * 3 * torch.cuda.get_device_properties(0).multi_processor_count:
+        pytest.skip("grid too small for the persistent form")
+    a = _run(ds, ts_lib, no_persist=False)
+    b = _run(ds, ts_lib, no_persist=True)
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16)) and torch.equal(a[1], b[1])
+    ds.out.copy_(a[0])
+    ds.lse.copy_(a[1])
+    assert_attention_close(ds.out, ds.lse, oracle_attention(wl, oracle_metadata(wl)), spec.name)
