@@ -99,16 +99,6 @@ constexpr float kMaxSlack = PA_MAX_SLACK;
 #ifndef PA_MASK_FAST
 #define PA_MASK_FAST 1
 #endif
-// int8 V enters the PV product still biased by +1152 (no per-element subtract); the
-// bias is removed from the output every kBiasPeriod chunks (and at the end) using the
-// column sums of the fp16 weights, which keeps the fp32 rounding of the biased sums
-// small next to the output.
-constexpr int kBiasPeriod = 16;
-// 1: subtract the bias from the fp16 codes before the PV product instead (exact codes,
-// one fp16x2 subtract per register, no column-sum MMA).
-#ifndef PA_INT8_V_EXACT
-#define PA_INT8_V_EXACT 1
-#endif
 // 1: the PV weights enter as two MMA operands, the weight rounded to the operand type
 // and its rounding residual rounded again (bf16: ~2^-16 relative, fp16: ~2^-22), which
 // keeps the output error well inside the output's own rounding; 0: one operand.
@@ -768,17 +758,10 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
   for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
-  // int8: per column, the sum of the fp16 weights that entered the PV product since the
-  // last bias removal (every row of the fragment holds the same sums); O = O_biased -
-  // 1152 sum.
-  constexpr bool kVBias = kQuant && !PA_INT8_V_EXACT;
-  float wsum[kNT][4];
-#pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) wsum[nt][0] = wsum[nt][1] = wsum[nt][2] = wsum[nt][3] = 0.f;
   // int8: the fp16 PV weights are p * v_scale * vmul, with vmul a warp-uniform power of
   // two that puts the largest V scale seen so far in [64, 128): weights stay below
   // 2^kMaxSlack * 128 (no fp16 overflow) and every weight within 2^-20 of the largest
-  // one is a normal fp16 number (no subnormal rounding).  o and wsum are in those units;
+  // one is a normal fp16 number (no subnormal rounding).  o is in those units;
   // vmul only shrinks (exact rescale) when a larger scale appears; it starts at 2^100,
   // so the first slice with a nonzero scale sets it.
   float vmul = 0x1p100f;
@@ -922,14 +905,11 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
             if (vmul_new < vmul) {
               const float r = vmul_new / vmul;  // a power of two: exact
 #pragma unroll
-              for (int nt = 0; nt < kNT; ++nt) {
+              for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
 #pragma unroll
                   for (int r4 = 0; r4 < 4; ++r4) o[nt][i][r4] *= r;
-#pragma unroll
-                for (int r4 = 0; r4 < 4; ++r4) wsum[nt][r4] *= r;
-              }
             }
             if (vmul_new < vmul) vmul = vmul_new;
           }
@@ -995,12 +975,6 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
               o[nt][i][2] *= alpha[0];
               o[nt][i][3] *= alpha[1];
             }
-            if constexpr (kVBias) {
-              wsum[nt][0] *= alpha[0];
-              wsum[nt][1] *= alpha[1];
-              wsum[nt][2] *= alpha[0];
-              wsum[nt][3] *= alpha[1];
-            }
           }
         }
 #pragma unroll
@@ -1056,28 +1030,18 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
             const uint32_t xa = x[2 * h] ^ 0x80808080u, xb = x[2 * h + 1] ^ 0x80808080u;
             uint32_t a[4] = {biased_bytes_to_f16x2(xa, 0x4240), biased_bytes_to_f16x2(xa, 0x4341),
                              biased_bytes_to_f16x2(xb, 0x4240), biased_bytes_to_f16x2(xb, 0x4341)};
-            if constexpr (!kVBias) {
+            // exact codes: the +1152 comes off in fp16 (an integer below 2048)
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&a[u]),
-                                          __floats2half2_rn(1152.f, 1152.f));
-                a[u] = *reinterpret_cast<const uint32_t*>(&v);
-              }
+            for (int u = 0; u < 4; ++u) {
+              const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&a[u]),
+                                        __floats2half2_rn(1152.f, 1152.f));
+              a[u] = *reinterpret_cast<const uint32_t*>(&v);
             }
 #pragma unroll
             for (int nt = 0; nt < kNT; ++nt) {
               mma16816<true>(o[nt][2 * ii + h], a, pb[nt][0], pb[nt][1]);
               if constexpr (PA_P_SPLIT) mma16816<true>(o[nt][2 * ii + h], a, pl[nt][0], pl[nt][1]);
             }
-          }
-        }
-        if constexpr (kVBias) {
-          // column sums of the fp16 weights: an all-ones A operand (fp16 1.0 = 0x3C00)
-          const uint32_t ones[4] = {0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u};
-#pragma unroll
-          for (int nt = 0; nt < kNT; ++nt) {
-            mma16816<true>(wsum[nt], ones, pb[nt][0], pb[nt][1]);
-            if constexpr (PA_P_SPLIT) mma16816<true>(wsum[nt], ones, pl[nt][0], pl[nt][1]);
           }
         }
       } else {
@@ -1103,19 +1067,6 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
     __syncwarp();
     // (the persistent form keeps the item's last stage for the merge below)
     if (lane == 0 && !(kPersist && c == n_chunks - 1)) mbar_arrive(&empty[stage]);
-    if constexpr (kVBias) {
-      if (c % kBiasPeriod == kBiasPeriod - 1) {
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int r4 = 0; r4 < 4; ++r4) o[nt][i][r4] -= 1152.f * wsum[nt][r4];
-#pragma unroll
-          for (int r4 = 0; r4 < 4; ++r4) wsum[nt][r4] = 0.f;
-        }
-      }
-    }
   }
 
   if (!kPersist) {  // (the persistent form signals once its CTA has no item left)
@@ -1184,11 +1135,7 @@ __global__ void __launch_bounds__(threads_of<NG>(), MINB)
         float* dst = red + (warp * 8 * kNT + head) * kRedStride;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          float v0 = o[nt][i][e], v1 = o[nt][i][2 + e];
-          if constexpr (kVBias) {
-            v0 -= 1152.f * wsum[nt][e];
-            v1 -= 1152.f * wsum[nt][2 + e];
-          }
+          const float v0 = o[nt][i][e], v1 = o[nt][i][2 + e];
           if constexpr (kQuant) {  // channels 16i + 2gid and the next one: one 8-byte store
             *reinterpret_cast<float2*>(dst + 16 * i + 2 * gid) = make_float2(v0 * scale, v1 * scale);
           } else {  // channels 16i + gid and 16i + gid + 8
