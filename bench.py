@@ -368,8 +368,8 @@ def pdl_study(torch, synthetic, DeviceStep, stream, replays=300, steps_per_graph
             g = capture(torch, steps, stream)
             for _ in range(3):
                 time_graph(torch, g, 20, stream)
-            row["graph_pdl_us" if pdl else "graph_us"] = min(
-                time_graph(torch, g, replays, stream) for _ in range(3)) / steps_per_graph
+            row["graph_pdl_us" if pdl else "graph_us"] = statistics.median(
+                time_graph(torch, g, replays, stream) for _ in range(5)) / steps_per_graph
             del g
             with torch.cuda.stream(stream):
                 for _ in range(50):
@@ -675,8 +675,8 @@ def measure_workload(torch, name, window, stream, steps, hbm_peak, peak_kind, l2
                 ds.step(use_pdl=pdl)
         g = capture(torch, run, stream)
         time_graph(torch, g, 5, stream)
-        row["graph_pdl_us" if pdl else "graph_us"] = min(
-            time_graph(torch, g, reps, stream) for _ in range(3)) / per_graph
+        row["graph_pdl_us" if pdl else "graph_us"] = statistics.median(
+            time_graph(torch, g, reps, stream) for _ in range(5)) / per_graph
         del g
     n = max(200, min(steps, 2000))
     with torch.cuda.stream(stream):
@@ -700,8 +700,8 @@ def measure_workload(torch, name, window, stream, steps, hbm_peak, peak_kind, l2
                 d.step(use_pdl=True)
         g = capture(torch, rotate, stream)
         time_graph(torch, g, 2, stream)
-        row["graph_pdl_l2_rotated_us"] = min(
-            time_graph(torch, g, max(5, reps // copies), stream) for _ in range(3)) / copies
+        row["graph_pdl_l2_rotated_us"] = statistics.median(
+            time_graph(torch, g, max(5, reps // copies), stream) for _ in range(5)) / copies
         row["l2_rotation_copies"] = copies
         del g, others, everyone
     best = row.get("graph_pdl_l2_rotated_us", row["graph_pdl_us"])
