@@ -653,7 +653,7 @@ def measure_workload(torch, name, window, stream, steps, hbm_peak, peak_kind, l2
     eager C-ABI calls with PDL.  Steps whose bytes fit in 2x the 129 MB L2 are also
     timed with the inputs rotated over enough copies to exceed 2x L2 (one graph stepping
     through every copy in turn).  with_producer: the producer launch alone and its
-    roofline; with_e2e: the end-to-end step through pa_decode_step_host."""
+    roofline; with_e2e: the end-to-end step with host-memory inputs and outputs (e2e_us)."""
     from paged_kv_decode_metadata_gb300 import binding, synthetic
     from paged_kv_decode_metadata_gb300.runtime import DeviceStep, WindowStep
 
