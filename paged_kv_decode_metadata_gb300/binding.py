@@ -509,14 +509,17 @@ def _decode_step_window_args(*, req_pool_indices, seq_lens, req_to_token, seqlen
 class PreparedCall:
     """One entry point with its arguments marshalled once: calling it repeats the call
     on the same tensors, stream and options, without re-validating or re-converting the
-    Python arguments (the tensors must stay alive and in place)."""
+    Python arguments.  The call holds references to the tensors it was prepared with
+    (``keep``), so their memory stays allocated; they must stay in place (in-place
+    updates are fine)."""
 
-    def __init__(self, name: str, args: tuple, lib=None):
+    def __init__(self, name: str, args: tuple, lib=None, keep: tuple = ()):
         self.lib = lib or load()
         self.name = name
         self.fn = getattr(self.lib, name)
         self.args = tuple(t(a) if a is not None else None
                           for t, a in zip(self.fn.argtypes, args))
+        self._keep = tuple(k for k in keep if isinstance(k, torch.Tensor))
 
     def __call__(self):
         st = self.fn(*self.args)
@@ -526,22 +529,22 @@ class PreparedCall:
 
 def prepare_decode_step(*, lib=None, **kw) -> PreparedCall:
     """``pa_decode_step`` with the given keyword arguments, marshalled once."""
-    return PreparedCall("pa_decode_step", _decode_step_args(**kw), lib)
+    return PreparedCall("pa_decode_step", _decode_step_args(**kw), lib, keep=tuple(kw.values()))
 
 
 def prepare_decode_step_host(*, lib=None, **kw) -> PreparedCall:
     """``pa_decode_step_host`` with the given keyword arguments, marshalled once."""
-    return PreparedCall("pa_decode_step_host", _decode_step_host_args(**kw), lib)
+    return PreparedCall("pa_decode_step_host", _decode_step_host_args(**kw), lib, keep=tuple(kw.values()))
 
 
 def prepare_decode_step_host_packed(*, lib=None, **kw) -> PreparedCall:
     """``pa_decode_step_host_packed`` with the given keyword arguments, marshalled once."""
-    return PreparedCall("pa_decode_step_host_packed", _decode_step_host_packed_args(**kw), lib)
+    return PreparedCall("pa_decode_step_host_packed", _decode_step_host_packed_args(**kw), lib, keep=tuple(kw.values()))
 
 
 def prepare_decode_step_window(*, lib=None, **kw) -> PreparedCall:
     """``pa_decode_step_window`` with the given keyword arguments, marshalled once."""
-    return PreparedCall("pa_decode_step_window", _decode_step_window_args(**kw), lib)
+    return PreparedCall("pa_decode_step_window", _decode_step_window_args(**kw), lib, keep=tuple(kw.values()))
 
 
 def pa_decode_step_static_scratch(*, req_pool_indices, seq_lens, req_to_token,
