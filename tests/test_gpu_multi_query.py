@@ -24,8 +24,10 @@ def lib():
     assert B.pa_read_error_flags(reset=True) == 0
 
 
-def _run_multi(wl, qlens, q, num_splits, use_pdl=True):
-    """GPU: metadata (with cu_seqlens_q from qlens), multi-query producer, reducer."""
+def _run_multi(wl, qlens, q, num_splits, use_pdl=True, host_io=False):
+    """GPU: metadata (with cu_seqlens_q from qlens), multi-query producer, reducer.
+    host_io: q, out and lse in pinned host memory (the kernels read and write them over
+    the host link)."""
     dev = "cuda"
     spec = wl.spec
     i32 = dict(dtype=torch.int32, device=dev)
@@ -42,13 +44,19 @@ def _run_multi(wl, qlens, q, num_splits, use_pdl=True):
     m = torch.empty((total_q, hq, num_splits), **f32)
     l = torch.empty((total_q, hq, num_splits), **f32)
     acc = torch.empty((total_q, hq, num_splits, d), **f32)
-    out = torch.empty((total_q, hq, d), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((total_q, hq), **f32)
+    if host_io:
+        out = torch.empty((total_q, hq, d), dtype=torch.bfloat16).pin_memory()
+        lse = torch.empty((total_q, hq), dtype=torch.float32).pin_memory()
+        q_in = q.contiguous().pin_memory()
+    else:
+        out = torch.empty((total_q, hq, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((total_q, hq), **f32)
+        q_in = q.to(dev)
     k = wl.k_cache.to(dev)
     v = wl.v_cache.to(dev)
     ks = wl.k_scale.to(dev) if wl.k_scale is not None else None
     vs = wl.v_scale.to(dev) if wl.v_scale is not None else None
-    B.pa_decode_splitk_multi(q.to(dev), k, v, pt, cl, cq, m, l, acc,
+    B.pa_decode_splitk_multi(q_in, k, v, pt, cl, cq, m, l, acc,
                              max_q_len=int(qlens.max()), max_seq_pages=msp,
                              num_splits=num_splits, sm_scale=wl.sm_scale, k_scale=ks, v_scale=vs,
                              use_pdl=use_pdl)
@@ -164,3 +172,17 @@ def test_multi_step_one_call_matches_stages(q_mode):
     torch.cuda.synchronize()
     assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
     assert_attention_close(out, lse, _oracle_multi(wl, qlens, q), f"step multi {q_mode}")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_multi_query_host_io_bit_identical(kv):
+    """q, out and lse in pinned host memory: the same bits as device buffers."""
+    spec = synthetic.Spec(f"mq_host_{kv}", bs=5, num_q_heads=16, num_kv_heads=4, num_pages=5 * 16,
+                          ragged=(200, 900), kv_dtype=kv, num_splits=3, seed=61)
+    wl = synthetic.make(spec)
+    qlens = synthetic.draw_query_lengths(spec.bs, 3, 62)
+    q = synthetic.draw_queries(int(qlens.sum()), spec.num_q_heads, spec.head_dim, 63)
+    a = _run_multi(wl, qlens, q, 3)
+    b = _run_multi(wl, qlens, q, 3, host_io=True)
+    assert torch.equal(a[0].cpu().view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1].cpu(), b[1])
